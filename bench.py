@@ -1,0 +1,385 @@
+"""Throughput of exact attention forward + backward on GB300.
+
+One step = fa_forward + fa_backward (its three stages: preprocess, dK/dV,
+dQ convert) over one batch of the Llama-shaped causal workload
+B=2, H=32, n=m=4096, d=128 (bf16 inputs, seeded N(0,1)), i.e. the whole hot
+path. The metric is fwd+bwd TFLOP/s counting 4*B*H*n*m*d per forward (halved
+under causal masking) and 2.5x that per backward.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own batch (independent heads, no
+collective on the data path: weak scaling); the timed region is bracketed by
+barriers and the max time over ranks is reported. Rank 0 prints one JSON line.
+
+--impl reference times the fp64 CPU oracle (tests' ground truth, not a
+product path) on the host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from exact_io_aware_27_gb300 import inputs as wl  # noqa: E402
+
+METRIC = "attention fwd+bwd TFLOP/s (bf16, causal) and % of GB300 dense BF16 peak"
+UNIT = "TFLOP/s"
+WORKLOAD = wl.LLAMA_B2_H32_N4096_D128
+L2_BYTES = 129 * 1024 * 1024
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "hbm_gbs": float(p["hbm_gbs"]), "source": "measured"}
+    except Exception:
+        return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0,
+                "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: torch.device):
+        self.proc = None
+        self.error = None
+        target = str(device.index or 0)
+        try:
+            uuid = torch.cuda.get_device_properties(device).uuid
+            target = "GPU-" + str(uuid)
+        except Exception:
+            pass
+        self.target = target
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.target, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception as e:  # no nvidia-smi
+            self.error = str(e)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "note": f"nvidia-smi unavailable: {self.error}"}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, power = [], [], []
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "no samples"}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+def _cpu_baseline(workload, heads: int):
+    """The oracle, as it stands, on `heads` full heads of the workload (rank 0)."""
+    import oracle
+    orc = oracle.default()
+    Q, K, V, dO = wl.workload_inputs(workload)
+    flat = [t.reshape(workload.heads, -1, workload.d) for t in (Q, K, V, dO)]
+    t0 = time.perf_counter()
+    for h in range(heads):
+        q, k, v, do = (t[h].double().numpy() for t in flat)
+        orc.forward(q, k, v, workload.causal)
+        orc.backward(q, k, v, do, workload.causal)
+    dt = time.perf_counter() - t0
+    flops = (workload.flops_fwd() + workload.flops_bwd()) * heads / workload.heads
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": orc.num_threads(),
+            "kind": "oracle",
+            "sample": f"{heads} of {workload.heads} heads ({workload.describe()}), full fp64 "
+                      f"forward + backward, {dt:.1f} s"}
+
+
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    import oracle
+    orc = oracle.default()
+    w = WORKLOAD
+    Q, K, V, dO = wl.workload_inputs(w)
+    flat = [t.reshape(w.heads, -1, w.d) for t in (Q, K, V, dO)]
+    # Each step: forward + backward of sampled query / key rows of one head,
+    # sized so that warm-up + timed steps stay within about two minutes.
+    per_step = max(0.05, min(2.0, 120.0 / max(1, args.steps + args.warmup)))
+    rows = w.n
+    heads_cycle = wl.sample_indices(w.heads, w.heads, 5003)
+
+    def step(i, r):
+        h = heads_cycle[i % len(heads_cycle)]
+        q, k, v, do = (t[h].double().numpy() for t in flat)
+        if r >= w.n:
+            orc.forward(q, k, v, w.causal)
+            orc.backward(q, k, v, do, w.causal)
+        else:
+            idx = wl.sample_indices(w.n, r, 6000 + i)
+            orc.forward_rows(q, k, v, idx, w.causal)
+            orc.backward_rows(q, k, v, do, idx, idx, w.causal)
+
+    # calibrate the sample size on the first warm-up step
+    t0 = time.perf_counter()
+    step(0, rows)
+    t_full = time.perf_counter() - t0
+    if t_full > per_step:
+        rows = max(32, int(w.n * per_step / t_full))
+    for i in range(1, args.warmup):
+        step(i, rows)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i, rows)
+    dt = (time.perf_counter() - t0) / max(1, args.steps)
+    flops = (w.flops_fwd() + w.flops_bwd()) / w.heads * rows / w.n
+    value = flops / dt / 1e12
+    sample = (f"one head per step, {rows} of {w.n} query rows (and as many key rows) sampled, "
+              f"fp64 oracle forward + backward; flops counted as that share of the head")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.name, "shape": w.describe()},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": orc.num_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import exact_io_aware_27_gb300 as fa
+
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = WORKLOAD
+    B, H, n, m, d = w.B, w.H, w.n, w.m, w.d
+    Q, K, V, dO = wl.attention_inputs(B, H, n, m, d, w.seed + 17 * rank, w.qk_std)
+    q, k, v, do = (t.to(dev) for t in (Q, K, V, dO))
+    O = torch.empty_like(q)
+    L = torch.empty((B, H, n), dtype=torch.float32, device=dev)
+    dQ, dK, dV = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = fa.alloc_workspace(B, H, n, m, d, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        fa.fa_forward(q, k, v, w.causal, O=O, L=L)
+        if ev is not None:
+            ev[1].record(stream)
+        fa.fa_backward_preprocess(O, do, L, ws)
+        if ev is not None:
+            ev[2].record(stream)
+        fa.fa_backward_dkdv(q, k, v, do, ws, causal=w.causal, dK=dK, dV=dV)
+        if ev is not None:
+            ev[3].record(stream)
+        fa.fa_backward_dq(B, H, n, m, d, ws, dQ=dQ)
+        if ev is not None:
+            ev[4].record(stream)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    if fa.fa_get_device_status() != 0:
+        raise RuntimeError("device barrier timeout during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    clocks = ClockSampler(dev)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize(dev)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clk = clocks.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    stage = [0.0] * 4
+    for e in evs:
+        for j in range(4):
+            stage[j] += e[j].elapsed_time(e[j + 1])
+    stage = [s / args.steps for s in stage]
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    if fa.fa_get_device_status() != 0:
+        raise RuntimeError("device barrier timeout during the timed region")
+
+    ms_per_step = elapsed_ms / args.steps
+    flops_step = w.flops_fwd() + w.flops_bwd()
+    value = flops_step * world / (ms_per_step * 1e-3) / 1e12
+    peaks = _peaks()
+    peak = peaks["bf16_tflops_sustained"]
+
+    # Dominant kernel and its roofline.
+    names = ["forward", "bwd_preprocess", "bwd_dkdv", "bwd_dq_convert"]
+    flops = [w.flops_fwd(), 0.0, w.flops_bwd(), 0.0]
+    top = max(range(4), key=lambda j: stage[j])
+    if flops[top] > 0:
+        ach = flops[top] / (stage[top] * 1e-3) / 1e12
+        roof = {"kernel": names[top], "bound": "tensor", "achieved": ach, "peak": peak,
+                "unit": "TFLOP/s", "frac": ach / peak, "traffic": None,
+                "peak_kind": f"bf16 dense, sustained ({peaks['source']})"}
+    else:
+        roof = {"kernel": names[top], "bound": "hbm", "achieved": None, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": None, "traffic": None}
+    kernels = {}
+    for j, nm in enumerate(names):
+        entry = {"ms": stage[j]}
+        if flops[j] > 0:
+            entry["tflops"] = flops[j] / (stage[j] * 1e-3) / 1e12
+        kernels[nm] = entry
+    bpe = 2
+    pre_bytes = 2 * B * H * n * d * bpe + B * H * n * 4 * 3 + B * H * n * d * 4
+    kernels["bwd_preprocess"]["gbs"] = pre_bytes / (stage[1] * 1e-3) / 1e9
+    cvt_bytes = B * H * n * d * (4 + bpe)
+    kernels["bwd_dq_convert"]["gbs"] = cvt_bytes / (stage[3] * 1e-3) / 1e9
+
+    # End to end through the public API with host buffers: pinned host inputs
+    # copied in, forward + backward, every output copied back, each step.
+    hq, hk, hv, hdo = (t.pin_memory() for t in (Q, K, V, dO))
+    ho, hl = torch.empty_like(hq).pin_memory(), torch.empty((B, H, n), dtype=torch.float32).pin_memory()
+    hdq, hdk, hdv = (torch.empty_like(t).pin_memory() for t in (hq, hk, hv))
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+    d2h = sum(t.numel() * t.element_size() for t in (ho, hl, hdq, hdk, hdv))
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        do.copy_(hdo, non_blocking=True)
+        fa.fa_forward(q, k, v, w.causal, O=O, L=L)
+        fa.fa_backward(q, k, v, O, L, do, w.causal, dQ=dQ, dK=dK, dV=dV, workspace=ws)
+        ho.copy_(O, non_blocking=True)
+        hl.copy_(L, non_blocking=True)
+        hdq.copy_(dQ, non_blocking=True)
+        hdk.copy_(dK, non_blocking=True)
+        hdv.copy_(dV, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 50))
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    e2e_ms = a.elapsed_time(b) / e2e_steps
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = flops_step * world / (e2e_ms * 1e-3) / 1e12
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = _cpu_baseline(w, args.cpu_heads)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": w.name, "shape": w.describe(), "global_batch": B * world,
+                       "seq_len": n, "parallelism": f"independent heads x{world}",
+                       "l2": "inputs exceed L2 (Q,K,V,dO 256 MiB per step > 129 MB)"},
+            "pct_of_peak": 100.0 * value / world / peak,
+            "roofline": roof,
+            "kernels": kernels,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": 4 * args.steps,
+            "clocks": clk,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-heads", type=int, default=4,
+                    help="heads of the workload the oracle baseline times")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,232 @@
+"""ctypes binding of the C-ABI in ``include/fa.h`` (argument marshalling only).
+
+Every function here checks the Python-side arguments, allocates outputs with
+torch when the caller passes none, and calls the library function of the same
+name on the current torch CUDA stream. All attention arithmetic runs in the
+library's CUDA kernels; there is no CPU or PyTorch fallback: if the library
+is missing, or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+from . import _build
+
+LIBRARY = _build.LIBRARY
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = -1
+FA_ERR_UNSUPPORTED_HEAD_DIM = -2
+FA_ERR_MISALIGNED = -3
+FA_ERR_UNSUPPORTED_DEVICE = -4
+FA_ERR_WORKSPACE_TOO_SMALL = -5
+FA_ERR_CUDA = -6
+FA_ERR_DEVICE_TIMEOUT = -7
+
+# Every entry point of include/fa.h and include/fa_selftest.h with its ctypes
+# signature: (restype, argtypes).
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+_S = ctypes.c_size_t
+SIGNATURES = {
+    "fa_forward": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P]),
+    "fa_backward_workspace_size": (_S, [_I, _I, _I, _I, _I]),
+    "fa_backward": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P,
+                         _S, _P]),
+    "fa_backward_preprocess": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _S, _P]),
+    "fa_backward_dkdv": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _S, _P]),
+    "fa_backward_dq": (_I, [_I, _I, _I, _I, _I, _F, _P, _P, _S, _P]),
+    "fa_status_string": (ctypes.c_char_p, [_I]),
+    "fa_get_device_status": (_I, [ctypes.POINTER(_I)]),
+    "fa_version": (_I, []),
+    "fa_selftest_mma": (_I, [_I, _P, _P, _P, _P]),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class FAError(RuntimeError):
+    """A negative status returned by the library."""
+
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {status_string(status)} ({status})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library. Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIBRARY):
+                raise RuntimeError(
+                    f"CUDA library {LIBRARY} is not built; run "
+                    "`python -c 'import __graft_entry__ as g; g.build()'` first")
+            handle = ctypes.CDLL(LIBRARY)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(handle, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = handle
+        return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().fa_status_string(int(status)).decode()
+
+
+def version() -> int:
+    return int(lib().fa_version())
+
+
+def _check(fn: str, rc: int) -> None:
+    if rc != FA_OK:
+        raise FAError(fn, rc)
+
+
+def _stream(t: torch.Tensor, stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream(t.device).cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _bf16_4d(name, t):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous 4-D bf16 CUDA tensor [B,H,seq,d]")
+
+
+def _scale(scale, d):
+    return 1.0 / math.sqrt(d) if scale is None else float(scale)
+
+
+def fa_forward(Q, K, V, causal: bool = False, scale: float | None = None, O=None, L=None,
+               stream=None):
+    """O [B,H,n,d] bf16 and L [B,H,n] fp32 (natural-log logsumexp)."""
+    for name, t in (("Q", Q), ("K", K), ("V", V)):
+        _bf16_4d(name, t)
+    B, H, n, d = Q.shape
+    m = K.shape[2]
+    if K.shape != (B, H, m, d) or V.shape != (B, H, m, d):
+        raise ValueError("K and V must be [B,H,m,d] with Q's B, H and d")
+    if O is None:
+        O = torch.empty_like(Q)
+    if L is None:
+        L = torch.empty((B, H, n), dtype=torch.float32, device=Q.device)
+    rc = lib().fa_forward(Q.data_ptr(), K.data_ptr(), V.data_ptr(), B, H, n, m, d,
+                          int(bool(causal)), _scale(scale, d), O.data_ptr(), L.data_ptr(),
+                          _stream(Q, stream))
+    _check("fa_forward", rc)
+    return O, L
+
+
+def fa_backward_workspace_size(B: int, H: int, n: int, m: int, d: int) -> int:
+    return int(lib().fa_backward_workspace_size(B, H, n, m, d))
+
+
+def alloc_workspace(B, H, n, m, d, device) -> torch.Tensor:
+    size = fa_backward_workspace_size(B, H, n, m, d)
+    if size == 0:
+        raise ValueError("invalid sizes for the backward workspace")
+    return torch.empty(size, dtype=torch.uint8, device=device)
+
+
+def fa_backward(Q, K, V, O, L, dO, causal: bool = False, scale: float | None = None, dQ=None,
+                dK=None, dV=None, workspace=None, stream=None):
+    """dQ, dK, dV (bf16) for upstream gradient dO, given the forward's O and L."""
+    for name, t in (("Q", Q), ("K", K), ("V", V), ("O", O), ("dO", dO)):
+        _bf16_4d(name, t)
+    B, H, n, d = Q.shape
+    m = K.shape[2]
+    if L.dtype != torch.float32 or tuple(L.shape) != (B, H, n) or not L.is_contiguous():
+        raise ValueError("L must be a contiguous fp32 [B,H,n] CUDA tensor")
+    dQ = torch.empty_like(Q) if dQ is None else dQ
+    dK = torch.empty_like(K) if dK is None else dK
+    dV = torch.empty_like(V) if dV is None else dV
+    if workspace is None:
+        workspace = alloc_workspace(B, H, n, m, d, Q.device)
+    rc = lib().fa_backward(Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), L.data_ptr(),
+                           dO.data_ptr(), B, H, n, m, d, int(bool(causal)), _scale(scale, d),
+                           dQ.data_ptr(), dK.data_ptr(), dV.data_ptr(), workspace.data_ptr(),
+                           workspace.numel() * workspace.element_size(), _stream(Q, stream))
+    _check("fa_backward", rc)
+    return dQ, dK, dV
+
+
+def fa_backward_preprocess(O, dO, L, workspace, stream=None):
+    B, H, n, d = O.shape
+    rc = lib().fa_backward_preprocess(O.data_ptr(), dO.data_ptr(), L.data_ptr(), B, H, n, d,
+                                      workspace.data_ptr(), workspace.numel(),
+                                      _stream(O, stream))
+    _check("fa_backward_preprocess", rc)
+
+
+def fa_backward_dkdv(Q, K, V, dO, workspace, causal=False, scale=None, dK=None, dV=None,
+                     stream=None):
+    B, H, n, d = Q.shape
+    m = K.shape[2]
+    dK = torch.empty_like(K) if dK is None else dK
+    dV = torch.empty_like(V) if dV is None else dV
+    rc = lib().fa_backward_dkdv(Q.data_ptr(), K.data_ptr(), V.data_ptr(), dO.data_ptr(), B, H, n,
+                                m, d, int(bool(causal)), _scale(scale, d), dK.data_ptr(),
+                                dV.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                                _stream(Q, stream))
+    _check("fa_backward_dkdv", rc)
+    return dK, dV
+
+
+def fa_backward_dq(B, H, n, m, d, workspace, scale=None, dQ=None, stream=None):
+    if dQ is None:
+        dQ = torch.empty((B, H, n, d), dtype=torch.bfloat16, device=workspace.device)
+    rc = lib().fa_backward_dq(B, H, n, m, d, _scale(scale, d), dQ.data_ptr(),
+                              workspace.data_ptr(), workspace.numel(), _stream(dQ, stream))
+    _check("fa_backward_dq", rc)
+    return dQ
+
+
+def fa_get_device_status() -> int:
+    out = ctypes.c_int(0)
+    _check("fa_get_device_status", lib().fa_get_device_status(ctypes.byref(out)))
+    return int(out.value)
+
+
+def fa_selftest_mma(mode: int, A: torch.Tensor, B: torch.Tensor) -> torch.Tensor:
+    """One tcgen05 GEMM in the layout family ``mode`` (see include/fa_selftest.h)."""
+    N = 64 if mode >= 3 else 128
+    D = torch.empty((128, N), dtype=torch.float32, device=A.device)
+    rc = lib().fa_selftest_mma(int(mode), A.data_ptr(), B.data_ptr(), D.data_ptr(),
+                               torch.cuda.current_stream(A.device).cuda_stream)
+    if rc != 0:
+        raise RuntimeError(f"fa_selftest_mma failed ({rc})")
+    return D
+
+
+class FlashAttention(torch.autograd.Function):
+    """Autograd wrapper: the forward saves Q, K, V, O and L (no n x m tensor),
+    the backward returns dQ, dK, dV ("05_flash_attention.py", FlashAttention)."""
+
+    @staticmethod
+    def forward(ctx, Q, K, V, causal=False, scale=None):
+        O, L = fa_forward(Q, K, V, causal, scale)
+        ctx.save_for_backward(Q, K, V, O, L)
+        ctx.causal = bool(causal)
+        ctx.scale = scale
+        return O
+
+    @staticmethod
+    def backward(ctx, dO):
+        Q, K, V, O, L = ctx.saved_tensors
+        dQ, dK, dV = fa_backward(Q, K, V, O, L, dO.contiguous(), ctx.causal, ctx.scale)
+        return dQ, dK, dV, None, None
+
+
+def flash_attention(Q, K, V, causal: bool = False, scale: float | None = None):
+    return FlashAttention.apply(Q, K, V, causal, scale)

@@ -1,0 +1,65 @@
+// Declarations shared by the library's translation units (not installed).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace fa {
+
+// Rows of the fp32 workspace arrays (D, scaled L, dQ accumulator) per head:
+// n rounded up to a multiple of this, so that every tile the kernels touch is
+// in bounds and every row stride is a multiple of 16 bytes.
+constexpr int kWorkspaceRowAlign = 128;
+
+inline int round_up(int x, int a) { return (x + a - 1) / a * a; }
+inline int ceil_div(int x, int a) { return (x + a - 1) / a; }
+
+// cuTensorMapEncodeTiled, fetched from the driver at first use.
+CUresult encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, cuuint32_t rank,
+                           void* base, const cuuint64_t* dims, const cuuint64_t* strides_bytes,
+                           const cuuint32_t* box, CUtensorMapSwizzle swizzle);
+
+// bf16 [BH, rows, d] viewed as a 3-D tensor (d innermost), boxes of
+// 64 columns x box_rows rows with 128-byte swizzle; reads past `rows` in a
+// head are zero-filled.
+CUresult make_bf16_head_map(CUtensorMap* map, const void* base, int BH, int rows, int d,
+                            int box_rows);
+// fp32 [BH, cols] as a 2-D tensor, boxes of box_cols x 1, no swizzle.
+CUresult make_f32_row_map(CUtensorMap* map, const void* base, int BH, int cols, int box_cols);
+
+struct FwdArgs {
+  const void *Q, *K, *V;
+  void* O;
+  float* L;
+  int BH, n, m, d, causal;
+  float scale;
+};
+struct BwdArgs {
+  const void *Q, *K, *V, *O, *dO;
+  const float* L;
+  void *dQ, *dK, *dV;
+  float* ws_D;    // [BH, n_pad] fp32
+  float* ws_L2;   // [BH, n_pad] fp32, L * log2(e); +inf in the padding
+  float* ws_dQ;   // [BH, n_pad, d] fp32
+  int BH, n, m, d, n_pad, causal;
+  float scale;
+};
+
+// Kernel launches (return the launch's cudaError_t).
+cudaError_t launch_forward(const FwdArgs& a, cudaStream_t s);
+cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t s);
+cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t s);
+cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t s);
+
+// Read-and-clear of each translation unit's device status word.
+cudaError_t forward_read_status(unsigned int* out);
+cudaError_t bwd_read_status(unsigned int* out);
+
+// Test-only: one tcgen05 GEMM through the same TMA / descriptor paths the
+// attention kernels use (see fa_selftest.h).
+cudaError_t launch_selftest_mma(int mode, const void* A, const void* B, float* D,
+                                cudaStream_t s);
+
+}  // namespace fa

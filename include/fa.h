@@ -1,0 +1,134 @@
+/*
+ * Exact, IO-aware softmax attention for NVIDIA GB300 (sm_103a): C-ABI boundary.
+ *
+ * Operation (from "05_flash_attention.py", standard_attention and
+ * flash_attention_forward / flash_attention_backward, and the "Flash
+ * Attention" notes, sections 1.1 and 1.5):
+ *
+ *   forward   S = Q K^T * scale            (score tile, never written to memory)
+ *             causal: key k is visible from query q only when k <= q (top-left)
+ *             P = softmax(S) row-wise,  O = P V
+ *             L = m + log(l)               natural-log logsumexp of each score row
+ *   backward  for the loss gradient dO = dLoss/dO:
+ *             D = rowsum(dO o O),  P rebuilt as exp(S - L)
+ *             dV = P^T dO,  dP = dO V^T,  dS = P o (dP - D)
+ *             dQ = dS K * scale,  dK = dS^T Q * scale
+ *
+ * Layouts. Every tensor is dense and row-major ("contiguous"):
+ *   Q, dO, O, dQ : bf16 [B, H, n, d]        K, V, dK, dV : bf16 [B, H, m, d]
+ *   L            : fp32 [B, H, n]           (natural log)
+ * d must be 64 or 128. n, m, B, H >= 1; B*H <= 65535 and n, m <= 2^24.
+ * scale must be finite and > 0 (1/sqrt(d) is the usual choice).
+ * All arithmetic accumulates in fp32; O, dQ, dK, dV are rounded to bf16
+ * (round to nearest even).
+ *
+ * Pointers. Every pointer is a device pointer the caller owns (for example
+ * memory from torch). bf16 tensors and the workspace must be 16-byte aligned;
+ * L must be 4-byte aligned. Outputs must not overlap inputs. The library keeps
+ * no pointer after a call returns, allocates no device memory and does not
+ * synchronise: work is queued on `stream` (a cudaStream_t; NULL = the legacy
+ * default stream) and the call returns once it is queued.
+ *
+ * Errors. Argument errors are reported before anything is queued and leave the
+ * outputs untouched. A launch error maps to FA_ERR_CUDA. The kernels bound
+ * every wait on an on-chip barrier; a wait that runs out (about two seconds)
+ * makes the kernel stop early and record FA_ERR_DEVICE_TIMEOUT in a device
+ * status word, readable with fa_get_device_status() once the stream is
+ * synchronised. The outputs of such a call are undefined.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+
+/* Symbols of this header are the library's only exports. */
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = -1,          /* null pointer, bad size, bad scale, overlap */
+  FA_ERR_UNSUPPORTED_HEAD_DIM = -2, /* d not in {64, 128} */
+  FA_ERR_MISALIGNED = -3,           /* a pointer breaks the alignment rules above */
+  FA_ERR_UNSUPPORTED_DEVICE = -4,   /* current device is not compute capability 10.3 */
+  FA_ERR_WORKSPACE_TOO_SMALL = -5,  /* workspace_bytes < fa_backward_workspace_size() */
+  FA_ERR_CUDA = -6,                 /* a CUDA runtime / driver call failed */
+  FA_ERR_DEVICE_TIMEOUT = -7        /* a kernel gave up waiting on a barrier */
+} fa_status;
+
+/*
+ * Forward pass ("05_flash_attention.py", flash_attention_forward; the
+ * FlashAttention autograd wrapper's forward saves Q, K, V, O, L).
+ * Inputs Q [B,H,n,d], K and V [B,H,m,d] (bf16). Outputs O [B,H,n,d] (bf16) and
+ * L [B,H,n] (fp32, natural log). One kernel launch on `stream`.
+ * Returns FA_OK or a negative fa_status.
+ */
+FA_API int fa_forward(const void* Q, const void* K, const void* V, int B, int H, int n, int m,
+               int d, int causal, float scale, void* O, float* L, void* stream);
+
+/*
+ * Bytes of device workspace fa_backward needs: D and a pre-scaled copy of L
+ * (fp32 [B, H, n_pad] each) and an fp32 dQ accumulator [B, H, n_pad, d], with
+ * n_pad = n rounded up to a multiple of 128. Returns 0 for invalid sizes.
+ */
+FA_API size_t fa_backward_workspace_size(int B, int H, int n, int m, int d);
+
+/*
+ * Backward pass ("05_flash_attention.py", flash_attention_backward: the
+ * FlashAttention-2 recompute form). Inputs Q, K, V, the forward's O and L, and
+ * dO. Outputs dQ [B,H,n,d], dK and dV [B,H,m,d] (bf16). `workspace` is caller
+ * owned device memory of at least fa_backward_workspace_size() bytes; its
+ * contents on entry do not matter. Queues fa_backward_preprocess,
+ * fa_backward_dkdv and fa_backward_dq on `stream`, in that order.
+ */
+FA_API int fa_backward(const void* Q, const void* K, const void* V, const void* O, const float* L,
+                const void* dO, int B, int H, int n, int m, int d, int causal, float scale,
+                void* dQ, void* dK, void* dV, void* workspace, size_t workspace_bytes,
+                void* stream);
+
+/*
+ * The three stages of fa_backward, callable one by one (same arguments and
+ * rules as fa_backward; each must see the workspace the previous one wrote).
+ *
+ * fa_backward_preprocess: D = rowsum(dO o O) per query row (the first line of
+ *   flash_attention_backward), L * log2(e) for the recompute, and a zeroed
+ *   dQ accumulator, all into the workspace. Memory bound.
+ * fa_backward_dkdv: per key block, loop over query blocks; rebuild P from L,
+ *   accumulate dV = P^T dO and dK = dS^T Q * scale on chip and write them
+ *   once; add each block's dS K into the fp32 dQ accumulator.
+ * fa_backward_dq: dQ = bf16(accumulator * scale).
+ */
+FA_API int fa_backward_preprocess(const void* O, const void* dO, const float* L, int B, int H, int n,
+                           int d, void* workspace, size_t workspace_bytes, void* stream);
+FA_API int fa_backward_dkdv(const void* Q, const void* K, const void* V, const void* dO, int B, int H,
+                     int n, int m, int d, int causal, float scale, void* dK, void* dV,
+                     void* workspace, size_t workspace_bytes, void* stream);
+FA_API int fa_backward_dq(int B, int H, int n, int m, int d, float scale, void* dQ,
+                   const void* workspace, size_t workspace_bytes, void* stream);
+
+/* A static, human-readable name for a status code. Never NULL. */
+FA_API const char* fa_status_string(int status);
+
+/*
+ * Reads the device status word of the current device into *status_out
+ * (FA_OK, or FA_ERR_DEVICE_TIMEOUT if a kernel gave up waiting since the last
+ * read) and clears it. Synchronises with the device. Returns FA_OK or
+ * FA_ERR_CUDA / FA_ERR_INVALID_ARG.
+ */
+FA_API int fa_get_device_status(int* status_out);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+FA_API int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

@@ -79,6 +79,16 @@ class Oracle:
             _dptr, _dptr, _dptr, _dptr, ctypes.c_long, ctypes.c_long, ctypes.c_long,
             ctypes.c_int, ctypes.c_double, _dptr, _dptr, _dptr, _dptr]
         lib.oracle_attention_backward.restype = ctypes.c_int
+        _lp = ctypes.POINTER(ctypes.c_long)
+        lib.oracle_attention_forward_rows.argtypes = [
+            _dptr, _dptr, _dptr, ctypes.c_long, ctypes.c_long, ctypes.c_long, ctypes.c_int,
+            ctypes.c_double, _lp, ctypes.c_long, _dptr, _dptr]
+        lib.oracle_attention_forward_rows.restype = ctypes.c_int
+        lib.oracle_attention_backward_rows.argtypes = [
+            _dptr, _dptr, _dptr, _dptr, ctypes.c_long, ctypes.c_long, ctypes.c_long,
+            ctypes.c_int, ctypes.c_double, _lp, ctypes.c_long, _lp, ctypes.c_long, _dptr,
+            _dptr, _dptr, _dptr]
+        lib.oracle_attention_backward_rows.restype = ctypes.c_int
         self._lib = lib
         self.path = path
 
@@ -150,6 +160,45 @@ class Oracle:
                 raise ValueError("oracle_attention_backward: bad arguments")
         return (dQ.reshape(*lead, n, d), dK.reshape(*lead, m, d),
                 dV.reshape(*lead, m, d), D.reshape(*lead, n))
+
+
+    # -- sampled rows of one head -------------------------------------------
+    def forward_rows(self, Q, K, V, rows, causal=False, scale=None):
+        """O[rows] and L[rows] of one head (Q [n,d], K and V [m,d])."""
+        q, k, v = (np.ascontiguousarray(x, dtype=np.float64) for x in (Q, K, V))
+        n, d = q.shape
+        m = k.shape[0]
+        idx = np.ascontiguousarray(rows, dtype=np.int64)
+        scale = 1.0 / np.sqrt(d) if scale is None else scale
+        O = np.empty((idx.size, d))
+        L = np.empty(idx.size)
+        rc = self._lib.oracle_attention_forward_rows(
+            _as_ptr(q), _as_ptr(k), _as_ptr(v), n, m, d, int(bool(causal)), float(scale),
+            idx.ctypes.data_as(ctypes.POINTER(ctypes.c_long)), idx.size, _as_ptr(O), _as_ptr(L))
+        if rc != 0:
+            raise ValueError("oracle_attention_forward_rows: bad arguments")
+        return O, L
+
+    def backward_rows(self, Q, K, V, dO, q_rows, k_rows, causal=False, scale=None):
+        """dQ[q_rows], dK[k_rows], dV[k_rows] and D (all rows) of one head."""
+        q, k, v, do = (np.ascontiguousarray(x, dtype=np.float64) for x in (Q, K, V, dO))
+        n, d = q.shape
+        m = k.shape[0]
+        qi = np.ascontiguousarray(q_rows, dtype=np.int64)
+        ki = np.ascontiguousarray(k_rows, dtype=np.int64)
+        scale = 1.0 / np.sqrt(d) if scale is None else scale
+        dQ = np.empty((max(qi.size, 1), d))
+        dK = np.empty((max(ki.size, 1), d))
+        dV = np.empty((max(ki.size, 1), d))
+        D = np.empty(n)
+        lp = ctypes.POINTER(ctypes.c_long)
+        rc = self._lib.oracle_attention_backward_rows(
+            _as_ptr(q), _as_ptr(k), _as_ptr(v), _as_ptr(do), n, m, d, int(bool(causal)),
+            float(scale), qi.ctypes.data_as(lp), qi.size, ki.ctypes.data_as(lp), ki.size,
+            _as_ptr(dQ), _as_ptr(dK), _as_ptr(dV), _as_ptr(D))
+        if rc != 0:
+            raise ValueError("oracle_attention_backward_rows: bad arguments")
+        return dQ[:qi.size], dK[:ki.size], dV[:ki.size], D
 
 
 def default() -> Oracle:

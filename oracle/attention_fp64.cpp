@@ -26,8 +26,11 @@
 // a full score row per query, a two-pass max / log-sum-exp, no tiling and no
 // fusion. D is computed from its definition sum_j P_ij dP_ij, not from the
 // rowsum(dO o O) shortcut (the tests check that identity separately).
-// dK and dV are formed key by key in a second pass that recomputes P_ij from
-// the same definitions, so no reduction across threads is needed.
+// dQ is formed query row by query row and dK, dV key row by key row, each
+// recomputing P_ij from the same definitions, so no reduction across threads
+// is needed. The *_rows variants evaluate the same definitions on a chosen
+// subset of query / key rows (used for the long workloads); the full
+// functions are those variants called with every row.
 //
 // All arrays are one head, row-major: Q, dO, O, dQ are n x d; K, V, dK, dV are
 // m x d; L and D have n entries.
@@ -111,20 +114,24 @@ int oracle_online_softmax_stats(const double* x, long len, long block, double* m
   return 0;
 }
 
-// Forward of one head: O (n x d) and natural-log logsumexp L (n).
-int oracle_attention_forward(const double* Q, const double* K, const double* V, long n,
-                             long m, long d, int causal, double scale, double* O,
-                             double* L) {
-  if (!Q || !K || !V || !O || !L || n < 1 || m < 1 || d < 1) return -1;
+// Forward of one head on selected query rows: for r < nrows, row rows[r] of
+// O goes to O[r * d ...] and its natural-log logsumexp to L[r].
+int oracle_attention_forward_rows(const double* Q, const double* K, const double* V, long n,
+                                  long m, long d, int causal, double scale, const long* rows,
+                                  long nrows, double* O, double* L) {
+  if (!Q || !K || !V || !O || !L || !rows || n < 1 || m < 1 || d < 1 || nrows < 0) return -1;
+  for (long r = 0; r < nrows; ++r)
+    if (rows[r] < 0 || rows[r] >= n) return -1;
 #pragma omp parallel
   {
     std::vector<double> s(m);
 #pragma omp for schedule(dynamic, 4)
-    for (long i = 0; i < n; ++i) {
+    for (long r = 0; r < nrows; ++r) {
+      const long i = rows[r];
       for (long j = 0; j < m; ++j) s[j] = score(Q, K, d, i, j, causal, scale);
       const double Li = row_logsumexp(s.data(), m);
-      L[i] = Li;
-      double* Oi = O + i * d;
+      L[r] = Li;
+      double* Oi = O + r * d;
       for (long c = 0; c < d; ++c) Oi[c] = 0.0;
       for (long j = 0; j < m; ++j) {
         if (s[j] == kNegInf) continue;  // P_ij = 0 exactly
@@ -136,47 +143,76 @@ int oracle_attention_forward(const double* Q, const double* K, const double* V, 
   return 0;
 }
 
-// Backward of one head for the scalar f = sum(O o dO): dQ (n x d), dK, dV (m x d).
-// D_out (n entries) receives D_i = sum_j P_ij dP_ij when not NULL.
-int oracle_attention_backward(const double* Q, const double* K, const double* V,
-                              const double* dO, long n, long m, long d, int causal,
-                              double scale, double* dQ, double* dK, double* dV,
-                              double* D_out) {
-  if (!Q || !K || !V || !dO || !dQ || !dK || !dV || n < 1 || m < 1 || d < 1) return -1;
+// Forward of one head: O (n x d) and natural-log logsumexp L (n).
+int oracle_attention_forward(const double* Q, const double* K, const double* V, long n,
+                             long m, long d, int causal, double scale, double* O, double* L) {
+  if (n < 1) return -1;
+  std::vector<long> all(n);
+  for (long i = 0; i < n; ++i) all[i] = i;
+  return oracle_attention_forward_rows(Q, K, V, n, m, d, causal, scale, all.data(), n, O, L);
+}
+
+// Backward of one head for the scalar f = sum(O o dO), evaluated on selected
+// rows: dQ for query rows qrows[0..nq) (into dQ[r * d ...]) and dK, dV for key
+// rows krows[0..nk). D_out (n entries, all rows) receives D_i = sum_j P_ij dP_ij
+// when not NULL. L_i and D_i are always formed for every query row, since each
+// key's gradient sums over all of them.
+int oracle_attention_backward_rows(const double* Q, const double* K, const double* V,
+                                   const double* dO, long n, long m, long d, int causal,
+                                   double scale, const long* qrows, long nq, const long* krows,
+                                   long nk, double* dQ, double* dK, double* dV, double* D_out) {
+  if (!Q || !K || !V || !dO || n < 1 || m < 1 || d < 1 || nq < 0 || nk < 0) return -1;
+  if ((nq > 0 && (!qrows || !dQ)) || (nk > 0 && (!krows || !dK || !dV))) return -1;
+  for (long r = 0; r < nq; ++r)
+    if (qrows[r] < 0 || qrows[r] >= n) return -1;
+  for (long r = 0; r < nk; ++r)
+    if (krows[r] < 0 || krows[r] >= m) return -1;
   std::vector<double> Lrow(n), Drow(n);
 
-  // Pass 1, query by query: L_i, D_i and dQ_i = scale * sum_j dS_ij K_j.
+  // Pass 1, every query row: L_i and D_i = sum_j P_ij dP_ij, dP_ij = <dO_i, V_j>.
 #pragma omp parallel
   {
-    std::vector<double> s(m), p(m), dp(m);
+    std::vector<double> s(m);
 #pragma omp for schedule(dynamic, 4)
     for (long i = 0; i < n; ++i) {
       for (long j = 0; j < m; ++j) s[j] = score(Q, K, d, i, j, causal, scale);
       const double Li = row_logsumexp(s.data(), m);
       double Di = 0.0;
       for (long j = 0; j < m; ++j) {
-        p[j] = (s[j] == kNegInf) ? 0.0 : std::exp(s[j] - Li);
-        double acc = 0.0;  // dP_ij = <dO_i, V_j>
-        for (long c = 0; c < d; ++c) acc += dO[i * d + c] * V[j * d + c];
-        dp[j] = acc;
-        Di += p[j] * dp[j];
+        if (s[j] == kNegInf) continue;
+        const double p = std::exp(s[j] - Li);
+        double dp = 0.0;
+        for (long c = 0; c < d; ++c) dp += dO[i * d + c] * V[j * d + c];
+        Di += p * dp;
       }
       Lrow[i] = Li;
       Drow[i] = Di;
-      double* dQi = dQ + i * d;
-      for (long c = 0; c < d; ++c) dQi[c] = 0.0;
-      for (long j = 0; j < m; ++j) {
-        const double dS = p[j] * (dp[j] - Di);
-        for (long c = 0; c < d; ++c) dQi[c] += scale * dS * K[j * d + c];
-      }
     }
   }
 
-  // Pass 2, key by key: dV_j = sum_i P_ij dO_i and dK_j = scale * sum_i dS_ij Q_i.
+  // Selected query rows: dQ_i = scale * sum_j dS_ij K_j, dS_ij = P_ij (dP_ij - D_i).
 #pragma omp parallel for schedule(dynamic, 4)
-  for (long j = 0; j < m; ++j) {
-    double* dKj = dK + j * d;
-    double* dVj = dV + j * d;
+  for (long r = 0; r < nq; ++r) {
+    const long i = qrows[r];
+    double* dQi = dQ + r * d;
+    for (long c = 0; c < d; ++c) dQi[c] = 0.0;
+    for (long j = 0; j < m; ++j) {
+      const double sij = score(Q, K, d, i, j, causal, scale);
+      if (sij == kNegInf) continue;
+      const double p = std::exp(sij - Lrow[i]);
+      double dp = 0.0;
+      for (long c = 0; c < d; ++c) dp += dO[i * d + c] * V[j * d + c];
+      const double dS = p * (dp - Drow[i]);
+      for (long c = 0; c < d; ++c) dQi[c] += scale * dS * K[j * d + c];
+    }
+  }
+
+  // Selected key rows: dV_j = sum_i P_ij dO_i and dK_j = scale * sum_i dS_ij Q_i.
+#pragma omp parallel for schedule(dynamic, 4)
+  for (long r = 0; r < nk; ++r) {
+    const long j = krows[r];
+    double* dKj = dK + r * d;
+    double* dVj = dV + r * d;
     for (long c = 0; c < d; ++c) dKj[c] = dVj[c] = 0.0;
     for (long i = 0; i < n; ++i) {
       const double sij = score(Q, K, d, i, j, causal, scale);
@@ -193,6 +229,19 @@ int oracle_attention_backward(const double* Q, const double* K, const double* V,
   }
   if (D_out) std::memcpy(D_out, Drow.data(), sizeof(double) * n);
   return 0;
+}
+
+// Backward of one head for the scalar f = sum(O o dO): dQ (n x d), dK, dV (m x d).
+int oracle_attention_backward(const double* Q, const double* K, const double* V,
+                              const double* dO, long n, long m, long d, int causal,
+                              double scale, double* dQ, double* dK, double* dV,
+                              double* D_out) {
+  if (n < 1 || m < 1) return -1;
+  std::vector<long> qa(n), ka(m);
+  for (long i = 0; i < n; ++i) qa[i] = i;
+  for (long j = 0; j < m; ++j) ka[j] = j;
+  return oracle_attention_backward_rows(Q, K, V, dO, n, m, d, causal, scale, qa.data(), n,
+                                        ka.data(), m, dQ, dK, dV, D_out);
 }
 
 }  // extern "C"

@@ -324,6 +324,27 @@ def pin_causal_nonsquare(orc):
         _close(Lc[i], Li[0], 1e-14, 1e-14, f"n<m causal row {i} L")
 
 
+# --------------------------------------------------------------------------
+# Sampled-row evaluation equals the same rows of the full evaluation
+# --------------------------------------------------------------------------
+def pin_sampled_rows(orc):
+    rng = _rng(11)
+    for (n, m, d, causal) in ((13, 11, 4, True), (9, 14, 3, False)):
+        Q, K, V, dO = (rng.standard_normal(s) for s in ((n, d), (m, d), (m, d), (n, d)))
+        O, L = orc.forward(Q, K, V, causal, 0.5)
+        dQ, dK, dV, D = orc.backward(Q, K, V, dO, causal, 0.5)
+        qr = np.array([n - 1, 0, 5, 2])
+        kr = np.array([3, m - 1, 0])
+        Os, Ls = orc.forward_rows(Q, K, V, qr, causal, 0.5)
+        _close(Os, O[qr], 1e-15, 1e-15, "sampled O")
+        _close(Ls, L[qr], 1e-15, 1e-15, "sampled L")
+        dQs, dKs, dVs, Ds = orc.backward_rows(Q, K, V, dO, qr, kr, causal, 0.5)
+        _close(dQs, dQ[qr], 1e-15, 1e-15, "sampled dQ")
+        _close(dKs, dK[kr], 1e-15, 1e-15, "sampled dK")
+        _close(dVs, dV[kr], 1e-15, 1e-15, "sampled dV")
+        _close(Ds, D, 1e-15, 1e-15, "sampled D")
+
+
 ALL_PINS = [pin_golden, pin_online_stats, pin_softmax_identity_v, pin_causal_row0,
             pin_zero_query, pin_single_key, pin_finite_differences, pin_invariants,
-            pin_torch_autograd, pin_tiled_page1, pin_causal_nonsquare]
+            pin_torch_autograd, pin_tiled_page1, pin_causal_nonsquare, pin_sampled_rows]

@@ -1,0 +1,115 @@
+"""Helpers for comparing the CUDA path with the fp64 oracle.
+
+Tolerances (fp32 accumulation, bf16 inputs and outputs):
+  O   max-abs error  <= 1e-2 beyond O's own rounding to bf16: the kernel must
+      return bf16, and rounding even the exact value costs up to half a bf16
+      ulp (2^-8 |O|, e.g. 0.0156 for |O| in [4, 8)), so each element may differ
+      from the fp64 value by 1e-2 + half_ulp_bf16(O_ref)
+  L   max-abs error  <= 2e-3   (natural log)
+  dQ, dK, dV  relative Frobenius error ||g - r||_F / ||r||_F <= 1e-2
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import exact_io_aware_27_gb300 as fa
+import oracle
+
+O_MAXABS = 1e-2
+L_MAXABS = 2e-3
+GRAD_REL = 1e-2
+
+
+def f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def half_ulp_bf16(x) -> np.ndarray:
+    """Half the bf16 spacing at |x| (8 significant bits): 2^(floor(log2|x|) - 8)."""
+    a = np.abs(np.asarray(x, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
+    return np.exp2(e - 8)
+
+
+def o_error(g, r) -> float:
+    """Max over elements of |g - r| in excess of r's own bf16 rounding."""
+    return float(np.max(np.abs(np.asarray(g) - r) - half_ulp_bf16(r)))
+
+
+def rel_fro(g, r) -> float:
+    den = float(np.linalg.norm(r))
+    num = float(np.linalg.norm(np.asarray(g, dtype=np.float64) - r))
+    return num / den if den > 0 else num
+
+
+def run_gpu(Q, K, V, dO, causal, scale=None, device="cuda"):
+    """Forward + backward through the C-ABI; returns fp64 numpy arrays."""
+    q, k, v, do = (t.to(device).contiguous() for t in (Q, K, V, dO))
+    O, L = fa.fa_forward(q, k, v, causal, scale)
+    dQ, dK, dV = fa.fa_backward(q, k, v, O, L, do, causal, scale)
+    torch.cuda.synchronize()
+    return {"O": f64(O), "L": f64(L), "dQ": f64(dQ), "dK": f64(dK), "dV": f64(dV)}
+
+
+def check_heads(Q, K, V, dO, causal, got, heads=None, scale=None):
+    """Full-row comparison on every head (or the listed flat head indices)."""
+    B, H, n, d = Q.shape
+    m = K.shape[2]
+    flat = [t.reshape(B * H, -1, d) for t in (Q, K, V, dO)]
+    g = {k: v.reshape(B * H, *v.shape[2:]) for k, v in got.items()}
+    heads = range(B * H) if heads is None else heads
+    report = {}
+    for h in heads:
+        q, k, v, do = (f64(t[h]) for t in flat)
+        O_r, L_r = oracle.forward(q, k, v, causal, scale)
+        dQ_r, dK_r, dV_r, _ = oracle.backward(q, k, v, do, causal, scale)
+        errs = {
+            "O": o_error(g["O"][h], O_r),
+            "O_raw": float(np.max(np.abs(g["O"][h] - O_r))),
+            "L": float(np.max(np.abs(g["L"][h] - L_r))),
+            "dQ": rel_fro(g["dQ"][h], dQ_r),
+            "dK": rel_fro(g["dK"][h], dK_r),
+            "dV": rel_fro(g["dV"][h], dV_r),
+        }
+        for key, val in errs.items():
+            report[key] = max(report.get(key, 0.0), val)
+    assert_within(report)
+    return report
+
+
+def check_sampled(Q, K, V, dO, causal, got, heads, q_rows, k_rows, scale=None):
+    """Sampled rows of sampled heads (for workloads the full oracle is too slow on)."""
+    B, H, n, d = Q.shape
+    flat = [t.reshape(B * H, -1, d) for t in (Q, K, V, dO)]
+    g = {k: v.reshape(B * H, *v.shape[2:]) for k, v in got.items()}
+    orc = oracle.default()
+    report = {}
+    for h in heads:
+        q, k, v, do = (f64(t[h]) for t in flat)
+        O_r, L_r = orc.forward_rows(q, k, v, q_rows, causal, scale)
+        dQ_r, dK_r, dV_r, _ = orc.backward_rows(q, k, v, do, q_rows, k_rows, causal, scale)
+        errs = {
+            "O": o_error(g["O"][h][q_rows], O_r),
+            "O_raw": float(np.max(np.abs(g["O"][h][q_rows] - O_r))),
+            "L": float(np.max(np.abs(g["L"][h][q_rows] - L_r))),
+            "dQ": rel_fro(g["dQ"][h][q_rows], dQ_r),
+            "dK": rel_fro(g["dK"][h][k_rows], dK_r),
+            "dV": rel_fro(g["dV"][h][k_rows], dV_r),
+        }
+        for key, val in errs.items():
+            report[key] = max(report.get(key, 0.0), val)
+    assert_within(report)
+    return report
+
+
+def assert_within(report):
+    bad = []
+    if not report["O"] <= O_MAXABS:
+        bad.append(f"O max-abs beyond bf16 output rounding {report['O']:.3e} > {O_MAXABS}")
+    if not report["L"] <= L_MAXABS:
+        bad.append(f"L max-abs {report['L']:.3e} > {L_MAXABS}")
+    for k in ("dQ", "dK", "dV"):
+        if not report[k] <= GRAD_REL:
+            bad.append(f"{k} rel-Frobenius {report[k]:.3e} > {GRAD_REL}")
+    assert not bad, "; ".join(bad) + f" (all: {report})"

@@ -1,0 +1,132 @@
+"""The C-ABI library on a machine without a GPU: it builds, loads, exports
+every symbol the public headers declare, and rejects bad arguments before any
+CUDA work (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_io_aware_27_gb300 as fa
+from exact_io_aware_27_gb300 import api
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fa.build()
+    return fa.lib()
+
+
+def _declared_symbols():
+    names = set()
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h)).read()
+            names |= set(re.findall(r"FA_(?:SELFTEST_)?API\s+[\w\s\*]*?\b(fa_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_symbols()
+    assert len(names) >= 10
+    for name in names:
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+    assert set(names) == set(api.SIGNATURES), "binding and headers disagree"
+
+
+def test_status_strings(lib):
+    for code in range(0, -8, -1):
+        s = fa.status_string(code)
+        assert s and s != "unknown status"
+    assert fa.status_string(-100) == "unknown status"
+    assert fa.version() >= 100
+
+
+def test_workspace_size(lib):
+    # D and scaled L (n_pad floats each) plus the dQ accumulator (n_pad * d floats)
+    assert fa.fa_backward_workspace_size(2, 3, 100, 50, 64) == 2 * 3 * 128 * (2 + 64) * 4
+    assert fa.fa_backward_workspace_size(1, 1, 128, 128, 128) == 128 * 130 * 4
+    assert fa.fa_backward_workspace_size(1, 1, 129, 7, 128) == 256 * 130 * 4
+    assert fa.fa_backward_workspace_size(1, 1, 0, 7, 128) == 0
+    assert fa.fa_backward_workspace_size(1, 1, 8, 7, 96) == 0
+
+
+FAKE = 1 << 20  # an aligned non-null address; never dereferenced (validation fails first)
+
+
+def _fwd(lib, Q=FAKE, K=FAKE + (1 << 24), V=FAKE + (2 << 24), B=1, H=1, n=8, m=8, d=64,
+         causal=0, scale=0.125, O=FAKE + (3 << 24), L=FAKE + (4 << 24)):
+    return lib.fa_forward(Q, K, V, B, H, n, m, d, causal, scale, O, L, None)
+
+
+def test_forward_argument_errors(lib):
+    assert _fwd(lib, Q=None) == api.FA_ERR_INVALID_ARG
+    assert _fwd(lib, L=None) == api.FA_ERR_INVALID_ARG
+    assert _fwd(lib, n=0) == api.FA_ERR_INVALID_ARG
+    assert _fwd(lib, m=-3) == api.FA_ERR_INVALID_ARG
+    assert _fwd(lib, B=0) == api.FA_ERR_INVALID_ARG
+    assert _fwd(lib, B=256, H=256) == api.FA_ERR_INVALID_ARG
+    assert _fwd(lib, d=96) == api.FA_ERR_UNSUPPORTED_HEAD_DIM
+    assert _fwd(lib, d=256) == api.FA_ERR_UNSUPPORTED_HEAD_DIM
+    assert _fwd(lib, scale=0.0) == api.FA_ERR_INVALID_ARG
+    assert _fwd(lib, scale=-1.0) == api.FA_ERR_INVALID_ARG
+    assert _fwd(lib, scale=float("nan")) == api.FA_ERR_INVALID_ARG
+    assert _fwd(lib, scale=float("inf")) == api.FA_ERR_INVALID_ARG
+    assert _fwd(lib, Q=FAKE + 2) == api.FA_ERR_MISALIGNED
+    assert _fwd(lib, O=FAKE + (3 << 24) + 8) == api.FA_ERR_MISALIGNED
+    assert _fwd(lib, L=FAKE + (4 << 24) + 2) == api.FA_ERR_MISALIGNED
+    assert _fwd(lib, O=FAKE) == api.FA_ERR_INVALID_ARG        # O overlaps Q
+    assert _fwd(lib, L=FAKE + (2 << 24) + 64) == api.FA_ERR_INVALID_ARG  # L overlaps V
+
+
+def test_forward_valid_arguments_reach_the_device_check(lib):
+    # Every argument is acceptable, so the call goes on to ask CUDA for the
+    # device: without a GPU that fails (FA_ERR_CUDA / unsupported device).
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _fwd(lib) in (api.FA_ERR_CUDA, api.FA_ERR_UNSUPPORTED_DEVICE)
+
+
+def test_backward_argument_errors(lib):
+    ws = fa.fa_backward_workspace_size(1, 1, 8, 8, 64)
+    base = [FAKE + (i << 24) for i in range(10)]
+
+    def bwd(**kw):
+        a = dict(Q=base[0], K=base[1], V=base[2], O=base[3], L=base[4], dO=base[5], B=1, H=1,
+                 n=8, m=8, d=64, causal=0, scale=0.125, dQ=base[6], dK=base[7], dV=base[8],
+                 ws=base[9], wsb=ws)
+        a.update(kw)
+        return lib.fa_backward(a["Q"], a["K"], a["V"], a["O"], a["L"], a["dO"], a["B"], a["H"],
+                               a["n"], a["m"], a["d"], a["causal"], a["scale"], a["dQ"], a["dK"],
+                               a["dV"], a["ws"], a["wsb"], None)
+
+    assert bwd(dO=None) == api.FA_ERR_INVALID_ARG
+    assert bwd(ws=None) == api.FA_ERR_INVALID_ARG
+    assert bwd(d=32) == api.FA_ERR_UNSUPPORTED_HEAD_DIM
+    assert bwd(wsb=ws - 4) == api.FA_ERR_WORKSPACE_TOO_SMALL
+    assert bwd(dK=base[7] + 2) == api.FA_ERR_MISALIGNED
+    assert bwd(ws=base[9] + 4) == api.FA_ERR_MISALIGNED
+    assert bwd(dQ=base[0]) == api.FA_ERR_INVALID_ARG           # dQ overlaps Q
+    assert bwd(dV=base[7]) == api.FA_ERR_INVALID_ARG           # dV overlaps dK
+    assert bwd(ws=base[6]) == api.FA_ERR_INVALID_ARG           # workspace overlaps dQ
+    assert bwd(scale=0.0) == api.FA_ERR_INVALID_ARG
+
+
+def test_device_status_needs_pointer(lib):
+    assert lib.fa_get_device_status(None) == api.FA_ERR_INVALID_ARG
+
+
+def test_python_binding_rejects_cpu_tensors(lib):
+    import torch
+    x = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.fa_forward(x, x, x)
+
+
+def test_selftest_argument_errors(lib):
+    assert lib.fa_selftest_mma(7, FAKE, FAKE, FAKE, None) == -1
+    assert lib.fa_selftest_mma(0, None, FAKE, FAKE, None) == -1
+    assert lib.fa_selftest_mma(0, FAKE + 2, FAKE, FAKE, None) == -3

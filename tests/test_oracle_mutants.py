@@ -14,8 +14,8 @@ import oracle
 from tests import oracle_pins
 
 MUTANTS = {
-    "dS_sign": ("const double dS = p[j] * (dp[j] - Di);",
-                "const double dS = p[j] * (dp[j] + Di);"),
+    "dS_sign": ("const double dS = p * (dp - Drow[i]);",
+                "const double dS = p * (dp + Drow[i]);"),
     "causal_off_by_one": ("if (causal && j > i) return kNegInf;",
                           "if (causal && j > i + 1) return kNegInf;"),
     "lse_drops_max": ("return mx + std::log(sum);", "return std::log(sum);"),
@@ -24,7 +24,7 @@ MUTANTS = {
     "dK_drops_scale": ("dKj[c] += scale * dS * Q[i * d + c];", "dKj[c] += dS * Q[i * d + c];"),
     "score_index_reversed": ("acc += Q[i * d + c] * K[j * d + c];",
                              "acc += Q[i * d + c] * K[j * d + (d - 1 - c)];"),
-    "D_drops_P": ("Di += p[j] * dp[j];", "Di += dp[j];"),
+    "D_drops_P": ("Di += p * dp;", "Di += dp;"),
     "dQ_wrong_operand": ("dQi[c] += scale * dS * K[j * d + c];",
                          "dQi[c] += scale * dS * Q[i * d + c];"),
     "O_wrong_weight": ("Oi[c] += p * V[j * d + c];", "Oi[c] += std::exp(s[j]) * V[j * d + c];"),
@@ -35,9 +35,9 @@ MUTANTS = {
 def test_mutant_is_caught(name, tmp_path):
     before, after = MUTANTS[name]
     src = open(oracle.SOURCE).read()
-    assert src.count(before) == 1, f"mutation site for {name} not found exactly once"
+    assert src.count(before) >= 1, f"mutation site for {name} not found"
     mutated = tmp_path / f"mutant_{name}.cpp"
-    mutated.write_text(src.replace(before, after))
+    mutated.write_text(src.replace(before, after))  # every occurrence
     lib = oracle.build(force=True, src=str(mutated), out=str(tmp_path / f"lib_{name}.so"))
     orc = oracle.Oracle(lib)
     caught = []
