@@ -240,7 +240,7 @@ def run_ours(args):
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     clocks = ClockSampler(dev)
     clocks.start()
-    time.sleep(0.3)
+    time.sleep(0.2)
     barrier()
     torch.cuda.synchronize(dev)
     t_start = torch.cuda.Event(enable_timing=True)
@@ -369,7 +369,7 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=600)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
