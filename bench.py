@@ -46,6 +46,26 @@ def _dist():
     return world, rank, local
 
 
+def rank_seed(w, rank: int) -> int:
+    """Seed of rank `rank`'s batch: every rank draws its own independent heads."""
+    return w.seed + 17 * rank
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """The maximum of `x` over all ranks (identity without a process group)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_value(flops_per_rank_step: float, world: int, ms_per_step: float) -> float:
+    """Whole-job TFLOP/s: every rank's FLOPs over the slowest rank's time."""
+    return flops_per_rank_step * world / (ms_per_step * 1e-3) / 1e12
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -202,7 +222,7 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     w = WORKLOAD
     B, H, n, m, d = w.B, w.H, w.n, w.m, w.d
-    Q, K, V, dO = wl.attention_inputs(B, H, n, m, d, w.seed + 17 * rank, w.qk_std)
+    Q, K, V, dO = wl.attention_inputs(B, H, n, m, d, rank_seed(w, rank), w.qk_std)
     q, k, v, do = (t.to(dev) for t in (Q, K, V, dO))
     O = torch.empty_like(q)
     L = torch.empty((B, H, n), dtype=torch.float32, device=dev)
@@ -258,17 +278,13 @@ def run_ours(args):
         for j in range(4):
             stage[j] += e[j].elapsed_time(e[j + 1])
     stage = [s / args.steps for s in stage]
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dev)
     if fa.fa_get_device_status() != 0:
         raise RuntimeError("device barrier timeout during the timed region")
 
     ms_per_step = elapsed_ms / args.steps
     flops_step = w.flops_fwd() + w.flops_bwd()
-    value = flops_step * world / (ms_per_step * 1e-3) / 1e12
+    value = weak_value(flops_step, world, ms_per_step)
     peaks = _peaks()
     peak = peaks["bf16_tflops_sustained"]
 
@@ -296,46 +312,46 @@ def run_ours(args):
     cvt_bytes = B * H * n * d * (4 + bpe)
     kernels["bwd_dq_convert"]["gbs"] = cvt_bytes / (stage[3] * 1e-3) / 1e9
 
-    # End to end through the public API with host buffers: pinned host inputs
-    # copied in, forward + backward, every output copied back, each step.
-    hq, hk, hv, hdo = (t.pin_memory() for t in (Q, K, V, dO))
-    ho, hl = torch.empty_like(hq).pin_memory(), torch.empty((B, H, n), dtype=torch.float32).pin_memory()
-    hdq, hdk, hdv = (torch.empty_like(t).pin_memory() for t in (hq, hk, hv))
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
-    d2h = sum(t.numel() * t.element_size() for t in (ho, hl, hdq, hdk, hdv))
+    e2e = None
+    if not args.no_e2e:
+        # End to end through the public API with host buffers: pinned host inputs
+        # copied in, forward + backward, every output copied back, each step.
+        hq, hk, hv, hdo = (t.pin_memory() for t in (Q, K, V, dO))
+        ho, hl = torch.empty_like(hq).pin_memory(), torch.empty((B, H, n), dtype=torch.float32).pin_memory()
+        hdq, hdk, hdv = (torch.empty_like(t).pin_memory() for t in (hq, hk, hv))
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+        d2h = sum(t.numel() * t.element_size() for t in (ho, hl, hdq, hdk, hdv))
 
-    def e2e_step():
-        q.copy_(hq, non_blocking=True)
-        k.copy_(hk, non_blocking=True)
-        v.copy_(hv, non_blocking=True)
-        do.copy_(hdo, non_blocking=True)
-        fa.fa_forward(q, k, v, w.causal, O=O, L=L)
-        fa.fa_backward(q, k, v, O, L, do, w.causal, dQ=dQ, dK=dK, dV=dV, workspace=ws)
-        ho.copy_(O, non_blocking=True)
-        hl.copy_(L, non_blocking=True)
-        hdq.copy_(dQ, non_blocking=True)
-        hdk.copy_(dK, non_blocking=True)
-        hdv.copy_(dV, non_blocking=True)
+        def e2e_step():
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            do.copy_(hdo, non_blocking=True)
+            fa.fa_forward(q, k, v, w.causal, O=O, L=L)
+            fa.fa_backward(q, k, v, O, L, do, w.causal, dQ=dQ, dK=dK, dV=dV, workspace=ws)
+            ho.copy_(O, non_blocking=True)
+            hl.copy_(L, non_blocking=True)
+            hdq.copy_(dQ, non_blocking=True)
+            hdk.copy_(dK, non_blocking=True)
+            hdv.copy_(dV, non_blocking=True)
 
-    e2e_steps = max(3, min(args.steps, 50))
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize(dev)
-    barrier()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    b.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier()
-    e2e_ms = a.elapsed_time(b) / e2e_steps
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = flops_step * world / (e2e_ms * 1e-3) / 1e12
+        e2e_steps = max(3, min(args.steps, 50))
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        e2e_ms = a.elapsed_time(b) / e2e_steps
+        e2e_ms = max_over_ranks(e2e_ms, dev)
+        e2e_value = weak_value(flops_step, world, e2e_ms)
+        e2e = {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -353,8 +369,7 @@ def run_ours(args):
             "pct_of_peak": 100.0 * value / world / peak,
             "roofline": roof,
             "kernels": kernels,
-            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "e2e": e2e,
             "gpu_launches": 4 * args.steps,
             "clocks": clk,
             "cpu_baseline": cpu,
@@ -373,6 +388,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the end-to-end host-buffer loop (profiling runs)")
     ap.add_argument("--cpu-heads", type=int, default=4,
                     help="heads of the workload the oracle baseline times")
     args = ap.parse_args()
