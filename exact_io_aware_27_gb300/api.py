@@ -42,6 +42,8 @@ SIGNATURES = {
     "fa_backward_preprocess": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _S, _P]),
     "fa_backward_dkdv": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _S, _P]),
     "fa_backward_dq": (_I, [_I, _I, _I, _I, _I, _F, _P, _P, _S, _P]),
+    "fa_backward_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P,
+                                 _P, _P]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_get_device_status": (_I, [ctypes.POINTER(_I)]),
     "fa_version": (_I, []),
@@ -158,6 +160,30 @@ def fa_backward(Q, K, V, O, L, dO, causal: bool = False, scale: float | None = N
                            dQ.data_ptr(), dK.data_ptr(), dV.data_ptr(), workspace.data_ptr(),
                            workspace.numel() * workspace.element_size(), _stream(Q, stream))
     _check("fa_backward", rc)
+    return dQ, dK, dV
+
+
+NOALLOC_WORKSPACE_BYTES = 32 * 1024 * 1024
+
+
+def fa_backward_noalloc(Q, K, V, O, L, dO, causal: bool = False, scale: float | None = None,
+                        dQ=None, dK=None, dV=None, stream=None):
+    """fa_backward using the library's static device workspace instead of a
+    caller buffer (for callers that cannot allocate device memory; limited to
+    problems whose workspace fits in NOALLOC_WORKSPACE_BYTES). Outputs are
+    allocated here only when not given."""
+    for name, t in (("Q", Q), ("K", K), ("V", V), ("O", O), ("dO", dO)):
+        _bf16_4d(name, t)
+    B, H, n, d = Q.shape
+    m = K.shape[2]
+    dQ = torch.empty_like(Q) if dQ is None else dQ
+    dK = torch.empty_like(K) if dK is None else dK
+    dV = torch.empty_like(V) if dV is None else dV
+    rc = lib().fa_backward_noalloc(Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(),
+                                   L.data_ptr(), dO.data_ptr(), B, H, n, m, d,
+                                   int(bool(causal)), _scale(scale, d), dQ.data_ptr(),
+                                   dK.data_ptr(), dV.data_ptr(), _stream(Q, stream))
+    _check("fa_backward_noalloc", rc)
     return dQ, dK, dV
 
 

@@ -113,6 +113,41 @@ FA_API int fa_backward_dkdv(const void* Q, const void* K, const void* V, const v
 FA_API int fa_backward_dq(int B, int H, int n, int m, int d, float scale, void* dQ,
                    const void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Backward pass without a caller-supplied workspace (the pages have no
+ * counterpart: this entry point exists only for callers that cannot allocate
+ * device memory). Same arguments, results and rules as fa_backward, minus
+ * `workspace` / `workspace_bytes`.
+ *
+ * Who needs it: code that owns no device allocator -- for example a plugin or
+ * custom operator loaded into a host program that keeps every byte of device
+ * memory to itself and offers no allocation hook, or a latency-critical caller
+ * that must not call cudaMalloc / cudaFree because they can synchronise the
+ * whole device. Such callers still pass their own inputs and outputs.
+ *
+ * Instead of a caller buffer it uses one statically sized array in device
+ * global memory inside this library: FA_NOALLOC_WORKSPACE_BYTES (32 MiB), held
+ * on every GPU that loads the library until the process exits. Problems whose
+ * workspace (fa_backward_workspace_size) exceeds it are rejected with
+ * FA_ERR_WORKSPACE_TOO_SMALL before anything is queued; for example
+ * B*H = 64 heads of n = 1024, d = 64 fit, but B*H = 64 heads of n = 4096,
+ * d = 128 do not. This call allocates nothing: no cudaMalloc, no cudaFree, no
+ * allocating library routine.
+ *
+ * The first call on a device looks up the array's device address on that
+ * device (one cudaGetSymbolAddress, with the device current) and caches it;
+ * make that first call before any stream capture. All calls share the one
+ * array, which keeps the previous call's contents; every call rewrites or
+ * clears all of it that it reads. Calls whose work overlaps on the GPU (for
+ * example on two streams without ordering between them) race on the array
+ * and give undefined results: order them on one stream or with events.
+ */
+#define FA_NOALLOC_WORKSPACE_BYTES (32u * 1024u * 1024u)
+FA_API int fa_backward_noalloc(const void* Q, const void* K, const void* V, const void* O,
+                               const float* L, const void* dO, int B, int H, int n, int m, int d,
+                               int causal, float scale, void* dQ, void* dK, void* dV,
+                               void* stream);
+
 /* A static, human-readable name for a status code. Never NULL. */
 FA_API const char* fa_status_string(int status);
 

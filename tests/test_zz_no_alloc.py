@@ -1,0 +1,70 @@
+"""fa_backward_noalloc: the backward pass for callers that cannot allocate
+device memory (a host program that owns every byte of device memory and
+offers no allocation hook, or a latency-critical caller that must avoid the
+device-wide synchronisation cudaMalloc / cudaFree can cause).
+
+It is checked, through the C-ABI, against fa_backward with a caller
+workspace on the same inputs, on two calls in a row (the static workspace
+keeps the first call's contents, so the second call shows that everything it
+reads is rewritten or cleared). This file is collected last on purpose.
+"""
+import ctypes
+
+import pytest
+import torch
+
+import exact_io_aware_27_gb300 as fa
+from exact_io_aware_27_gb300 import api
+from exact_io_aware_27_gb300 import inputs as wl
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-2  # the tests' gradient tolerance (relative Frobenius error)
+
+
+def _rel(a, b):
+    a, b = a.double(), b.double()
+    return float((a - b).norm() / b.norm().clamp_min(1e-30))
+
+
+def _noalloc_c(q, k, v, O, L, do, causal, dQ, dK, dV):
+    B, H, n, d = q.shape
+    m = k.shape[2]
+    return fa.lib().fa_backward_noalloc(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), O.data_ptr(), L.data_ptr(), do.data_ptr(),
+        B, H, n, m, d, int(causal), ctypes.c_float(1.0 / d ** 0.5), dQ.data_ptr(),
+        dK.data_ptr(), dV.data_ptr(), torch.cuda.current_stream().cuda_stream)
+
+
+@pytest.mark.parametrize("B,H,n,m,d,causal,seed", [
+    (2, 3, 300, 300, 128, True, 8101),
+    (1, 4, 250, 700, 64, False, 8102),
+])
+def test_noalloc_matches_fa_backward_twice(B, H, n, m, d, causal, seed):
+    fa.build()
+    for call in range(2):
+        Q, K, V, dO = (t.cuda() for t in wl.attention_inputs(B, H, n, m, d, seed + call))
+        O, L = fa.fa_forward(Q, K, V, causal)
+        ref = fa.fa_backward(Q, K, V, O, L, dO, causal)
+        got = [torch.full_like(t, float("nan")) for t in ref]
+        rc = _noalloc_c(Q, K, V, O, L, dO, causal, *got)
+        torch.cuda.synchronize()
+        assert rc == 0, fa.status_string(rc)
+        for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+            assert torch.isfinite(g.float()).all(), f"call {call}: {name} not fully written"
+            assert _rel(g, r) <= TOL, f"call {call}: {name} differs: {_rel(g, r):.3e}"
+        # dK and dV do not depend on accumulation order: identical bits
+        assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2])
+    assert fa.fa_get_device_status() == 0
+
+
+def test_noalloc_rejects_problems_larger_than_its_workspace():
+    fa.build()
+    B, H, n, m, d = 2, 32, 4096, 4096, 128
+    assert fa.fa_backward_workspace_size(B, H, n, m, d) > api.NOALLOC_WORKSPACE_BYTES
+    x = torch.empty(16, dtype=torch.bfloat16, device="cuda")
+    rc = fa.lib().fa_backward_noalloc(x.data_ptr(), x.data_ptr(), x.data_ptr(), x.data_ptr(),
+                                      x.data_ptr(), x.data_ptr(), B, H, n, m, d, 1,
+                                      ctypes.c_float(0.1), x.data_ptr(), x.data_ptr(),
+                                      x.data_ptr(), None)
+    assert rc == api.FA_ERR_WORKSPACE_TOO_SMALL
