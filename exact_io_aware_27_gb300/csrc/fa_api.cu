@@ -158,6 +158,14 @@ int prepare_backward(const void* Q, const void* K, const void* V, const void* O,
 
 }  // namespace
 
+int heads_per_group(int BH, int tiles_per_head) {
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int g = ceil_div(2 * sms, tiles_per_head > 0 ? tiles_per_head : 1);
+  return g < 1 ? 1 : (g > BH ? BH : g);
+}
+
 CUresult encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, cuuint32_t rank,
                            void* base, const cuuint64_t* dims, const cuuint64_t* strides_bytes,
                            const cuuint32_t* box, CUtensorMapSwizzle swizzle) {

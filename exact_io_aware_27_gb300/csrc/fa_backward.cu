@@ -21,9 +21,11 @@
 //               is added into the fp32 accumulator with global atomics.
 //   dq          dQ = bf16(accumulator * scale).
 //
-// dkdv roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer, warps 4..7
-// compute P^T and dS^T (thread = key row), warps 8..11 drain dQ from TMEM and
-// add it to global memory.
+// dkdv roles (512 threads): warp 0 TMA producer, warp 1 MMA issuer, warps 4..11
+// compute P^T and dS^T (two warpgroups, each owning half of the query columns;
+// thread = key row), warps 12..15 drain dQ from TMEM into global memory. The
+// MMA issue order is software-pipelined: S^T_i and dP^T_i are issued as soon as
+// the compute groups have read block i-1's, ahead of dV_{i-1}, dK_{i-1}, dQ_{i-1}.
 #include "fa_internal.h"
 #include "sm103.cuh"
 
@@ -39,6 +41,7 @@ template <int D>
 struct BwdCfg {
   static constexpr int BN = 128;                    // keys per CTA = TMEM lanes
   static constexpr int BQ = (D == 128) ? 64 : 128;  // queries per inner step
+  static constexpr int CW = BQ / 2;                 // query columns per compute warpgroup
   static constexpr int KCH = D / 64;
   static constexpr int KV_CHUNK = 128 * 128;        // one 64-column chunk of K or V
   static constexpr int KV_TILE = KCH * KV_CHUNK;
@@ -46,7 +49,7 @@ struct BwdCfg {
   static constexpr int Q_TILE = KCH * Q_CHUNK;
   static constexpr int DS_CHUNK = BN * 128;         // 64 queries x 128 keys of dS^T (bf16)
   static constexpr int DS_TILE = (BQ / 64) * DS_CHUNK;
-  static constexpr int STAGES = 2;
+  static constexpr int STAGES = 3;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + KV_TILE;
   static constexpr int OFF_Q = OFF_V + KV_TILE;
@@ -54,23 +57,25 @@ struct BwdCfg {
   static constexpr int OFF_DS = OFF_DO + STAGES * Q_TILE;
   static constexpr int OFF_LSE = OFF_DS + DS_TILE;          // [STAGES][BQ] fp32
   static constexpr int OFF_DD = OFF_LSE + STAGES * BQ * 4;  // [STAGES][BQ] fp32
-  static constexpr int OFF_BAR = OFF_DD + STAGES * BQ * 4;
+  static constexpr int OFF_DQS = OFF_DD + STAGES * BQ * 4;  // [BQ x D] fp32 dQ staging
+  static constexpr int DQS_BYTES = (D == 128) ? BQ * D * 4 : 0;
+  static constexpr int OFF_BAR = OFF_DQS + DQS_BYTES;
   // barrier slots
   static constexpr int B_KV = 0;
-  static constexpr int B_QF = 1;   // + stage
-  static constexpr int B_QE = 3;   // + stage
-  static constexpr int B_OF = 5;   // + stage
-  static constexpr int B_OE = 7;   // + stage
-  static constexpr int B_SF = 9;
-  static constexpr int B_SFREE = 10;
-  static constexpr int B_PF = 11;
-  static constexpr int B_DVD = 12;
-  static constexpr int B_DSF = 13;
-  static constexpr int B_DSD = 14;
-  static constexpr int B_DQE = 15;
-  static constexpr int B_ACC = 16;
-  static constexpr int B_DRAIN = 17;
-  static constexpr int NBAR = 18;
+  static constexpr int B_QF = 1;                // + stage
+  static constexpr int B_QE = B_QF + STAGES;    // + stage
+  static constexpr int B_OF = B_QE + STAGES;    // + stage
+  static constexpr int B_OE = B_OF + STAGES;    // + stage
+  static constexpr int B_SF = B_OE + STAGES;
+  static constexpr int B_SFREE = B_SF + 1;
+  static constexpr int B_PF = B_SF + 2;
+  static constexpr int B_DVD = B_SF + 3;
+  static constexpr int B_DSF = B_SF + 4;
+  static constexpr int B_DSD = B_SF + 5;
+  static constexpr int B_DQE = B_SF + 6;
+  static constexpr int B_ACC = B_SF + 7;
+  static constexpr int B_DRAIN = B_SF + 8;
+  static constexpr int NBAR = B_DRAIN + 1;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;
   // TMEM columns
   static constexpr uint32_t COL_S = 0;
@@ -80,7 +85,8 @@ struct BwdCfg {
   static constexpr uint32_t COL_DK = COL_DV + D;
   static constexpr uint32_t COL_DQ = COL_DK + D;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr int THREADS = 384;
+  static constexpr int THREADS = 512;
+  static constexpr int COMPUTE_THREADS = 256;
   static_assert(COL_DQ + 64 <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
@@ -88,7 +94,7 @@ struct BwdCfg {
 struct BwdParams {
   __nv_bfloat16 *dK, *dV;
   float* ws_dQ;
-  int n, m, n_pad, BH, causal;
+  int n, m, n_pad, BH, causal, ktiles, group;
   float scale, scale_log2;
 };
 
@@ -100,7 +106,7 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(512, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                 const __grid_constant__ CUtensorMap tmL2, const __grid_constant__ CUtensorMap tmD,
@@ -115,8 +121,10 @@ __global__ void __launch_bounds__(384, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int ktile = blockIdx.x / p.BH;  // key blocks near 0 carry the most work
-  const int bh = blockIdx.x % p.BH;
+  // Key blocks near 0 carry the most work under causal masking: rank 0 first,
+  // heads taken a group at a time so the blocks in flight share L2.
+  int ktile, bh;
+  grouped_tile(blockIdx.x, p.BH, p.ktiles, p.group, ktile, bh);
   const int ks = ktile * C::BN;
   const int nqb = (p.n + C::BQ - 1) / C::BQ;
   const int i_start = p.causal ? ks / C::BQ : 0;  // first block with a query q >= ks
@@ -131,10 +139,10 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&bar[C::B_OE + s], 1);
     }
     mbar_init(&bar[C::B_SF], 1);
-    mbar_init(&bar[C::B_SFREE], 128);
-    mbar_init(&bar[C::B_PF], 128);
+    mbar_init(&bar[C::B_SFREE], C::COMPUTE_THREADS);
+    mbar_init(&bar[C::B_PF], C::COMPUTE_THREADS);
     mbar_init(&bar[C::B_DVD], 1);
-    mbar_init(&bar[C::B_DSF], 128);
+    mbar_init(&bar[C::B_DSF], C::COMPUTE_THREADS);
     mbar_init(&bar[C::B_DSD], 1);
     mbar_init(&bar[C::B_DQE], 128);
     mbar_init(&bar[C::B_ACC], 1);
@@ -166,8 +174,8 @@ __global__ void __launch_bounds__(384, 1)
       }
       int nqi = 0, noi = 0;
       for (int i = 0; i < nq; ++i) {
-        const int s = i & 1;
-        const uint32_t ph = (i >> 1) & 1;
+        const int s = i % C::STAGES;
+        const uint32_t ph = (i / C::STAGES) & 1;
         const int q0 = (i_start + i) * C::BQ;
         if (i >= C::STAGES && !mbar_wait(&bar[C::B_QE + s], ph ^ 1, wc)) break;
         mbar_arrive_expect_tx(&bar[C::B_QF + s], C::Q_TILE + 2 * C::BQ * 4);
@@ -188,9 +196,9 @@ __global__ void __launch_bounds__(384, 1)
       }
       drain_wait(&bar[C::B_KV], 0);
       for (int i = max(0, nqi - C::STAGES); i < nqi; ++i)
-        drain_wait(&bar[C::B_QF + (i & 1)], (i >> 1) & 1);
+        drain_wait(&bar[C::B_QF + i % C::STAGES], (i / C::STAGES) & 1);
       for (int i = max(0, noi - C::STAGES); i < noi; ++i)
-        drain_wait(&bar[C::B_OF + (i & 1)], (i >> 1) & 1);
+        drain_wait(&bar[C::B_OF + i % C::STAGES], (i / C::STAGES) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -206,9 +214,9 @@ __global__ void __launch_bounds__(384, 1)
       bool ok = mbar_wait(&bar[C::B_KV], 0, wc);
       for (int i = 0; ok && i <= nq; ++i) {
         if (i < nq) {
-          // S^T = K Q_i^T and dP^T = V dO_i^T
-          const int s = i & 1;
-          const uint32_t ph = (i >> 1) & 1;
+          // S^T = K Q_i^T and dP^T = V dO_i^T, as soon as block i-1's are read
+          const int s = i % C::STAGES;
+          const uint32_t ph = (i / C::STAGES) & 1;
           if (!mbar_wait(&bar[C::B_QF + s], ph, wc)) break;
           if (!mbar_wait(&bar[C::B_OF + s], ph, wc)) break;
           if (i >= 1 && !mbar_wait(&bar[C::B_SFREE], (i - 1) & 1, wc)) break;
@@ -232,9 +240,21 @@ __global__ void __launch_bounds__(384, 1)
           umma_commit(&bar[C::B_SF]);
         }
         if (i >= 1) {
-          // dK += dS^T Q_{i-1} and this block's share of dQ_{i-1}
           const int ii = i - 1;
-          const int s = ii & 1;
+          const int s = ii % C::STAGES;
+          // dV += P^T dO_{i-1}
+          if (!mbar_wait(&bar[C::B_PF], ii & 1, wc)) break;
+          tc_fence_after();
+          const uint32_t sO = smem_u32(smem + C::OFF_DO + s * C::Q_TILE);
+#pragma unroll
+          for (int kk = 0; kk < C::BQ / 16; ++kk) {
+            umma_ts(tmem + C::COL_DV, tmem + C::COL_P + kk * 8,
+                    sdesc_sw128(sO + kk * 2048, C::Q_CHUNK, 1024), kIdescDV,
+                    (ii > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(&bar[C::B_DVD]);
+          umma_commit(&bar[C::B_OE + s]);
+          // dK += dS^T Q_{i-1} and this block's share of dQ_{i-1}
           if (!mbar_wait(&bar[C::B_DSF], ii & 1, wc)) break;
           if (ii >= 1 && !mbar_wait(&bar[C::B_DQE], (ii - 1) & 1, wc)) break;
           tc_fence_after();
@@ -259,106 +279,148 @@ __global__ void __launch_bounds__(384, 1)
           umma_commit(&bar[C::B_DSD]);
           umma_commit(&bar[C::B_QE + s]);
         }
-        if (i < nq) {
-          // dV += P^T dO_i
-          const int s = i & 1;
-          if (!mbar_wait(&bar[C::B_PF], i & 1, wc)) break;
-          tc_fence_after();
-          const uint32_t sO = smem_u32(smem + C::OFF_DO + s * C::Q_TILE);
-#pragma unroll
-          for (int kk = 0; kk < C::BQ / 16; ++kk) {
-            umma_ts(tmem + C::COL_DV, tmem + C::COL_P + kk * 8,
-                    sdesc_sw128(sO + kk * 2048, C::Q_CHUNK, 1024), kIdescDV,
-                    (i > 0 || kk > 0) ? 1u : 0u);
-          }
-          umma_commit(&bar[C::B_DVD]);
-          umma_commit(&bar[C::B_OE + s]);
-        }
       }
       umma_commit(&bar[C::B_ACC]);
       umma_commit(&bar[C::B_DRAIN]);
       drain_wait(&bar[C::B_DRAIN], 0);
     }
-  } else if (warp >= 4 && warp < 8) {
+  } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------ P^T, dS^T
-    const int krow = (warp - 4) * 32 + lane;
+    const int half = (warp - 4) >> 2;              // which half of the query columns
+    const int krow = ((warp - 4) & 3) * 32 + lane;  // key row = TMEM lane
     const int kg = ks + krow;
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const int c0 = half * C::CW;                   // first query column of this group
     const float sl2 = p.scale_log2;
     const bool key_ok = kg < p.m;
     const uint32_t sDS = smem_u32(smem + C::OFF_DS);
     bool ok = true;
     for (int i = 0; i < nq; ++i) {
-      const int s = i & 1;
+      const int s = i % C::STAGES;
       const int q0 = (i_start + i) * C::BQ;
-      if (!mbar_wait(&bar[C::B_QF + s], (i >> 1) & 1, wc)) { ok = false; break; }
-      if (!mbar_wait(&bar[C::B_SF], i & 1, wc)) { ok = false; break; }
+      if (!warp_wait(&bar[C::B_QF + s], (i / C::STAGES) & 1, wc)) { ok = false; break; }
+      if (!warp_wait(&bar[C::B_SF], i & 1, wc)) { ok = false; break; }
       tc_fence_after();
-      const float* lse = reinterpret_cast<const float*>(smem + C::OFF_LSE + s * C::BQ * 4);
-      const float* dd = reinterpret_cast<const float*>(smem + C::OFF_DD + s * C::BQ * 4);
-      // Causal: key kg is hidden from query q when kg > q.
-      const bool need_mask = p.causal && (ks + C::BN - 1 > q0);
-      const int qlim = kg - q0;  // columns c < qlim are hidden under causal masking
+      const float* lse = reinterpret_cast<const float*>(smem + C::OFF_LSE + s * C::BQ * 4) + c0;
+      const float* dd = reinterpret_cast<const float*>(smem + C::OFF_DD + s * C::BQ * 4) + c0;
+      // Causal: key kg is hidden from query q0 + c when c < kg - q0.
+      const bool need_mask = p.causal && (ks + C::BN - 1 > q0 + c0);
+      const int qlim = kg - q0 - c0;  // in this group's column numbering
 
-      uint32_t pp[C::BQ / 2];
-#pragma unroll
-      for (int c = 0; c < C::BQ / 32; ++c) {
-        uint32_t sr[32];
-        tmem_ld32(lane_base + C::COL_S + 32 * c, sr);
+      uint32_t pp[C::CW / 2];
+      if (C::CW == 32) {
+        // Read this group's S^T and dP^T columns, then release them at once so
+        // that the next block's S^T / dP^T products overlap this arithmetic.
+        uint32_t sr[32], dr[32];
+        tmem_ld32(lane_base + C::COL_S + c0, sr);
+        tmem_ld32(lane_base + C::COL_DP + c0, dr);
         tmem_ld_wait();
         reg_fence32(sr);
+        reg_fence32(dr);
+        tc_fence_before();
+        mbar_arrive(&bar[C::B_SFREE]);
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const int q = 32 * c + e;
-          float p0 = ex2(fmaf(__uint_as_float(sr[e]), sl2, -lse[q]));
-          float p1 = ex2(fmaf(__uint_as_float(sr[e + 1]), sl2, -lse[q + 1]));
+          const float2 l2 = *reinterpret_cast<const float2*>(lse + e);
+          float p0 = ex2(fmaf(__uint_as_float(sr[e]), sl2, -l2.x));
+          float p1 = ex2(fmaf(__uint_as_float(sr[e + 1]), sl2, -l2.y));
           if (need_mask) {
-            if (q < qlim) p0 = 0.f;
-            if (q + 1 < qlim) p1 = 0.f;
+            if (e < qlim) p0 = 0.f;
+            if (e + 1 < qlim) p1 = 0.f;
           }
           if (!key_ok) p0 = p1 = 0.f;
-          pp[16 * c + e / 2] = pack_bf16(p0, p1);
+          pp[e / 2] = pack_bf16(p0, p1);
         }
-      }
-      if (i >= 1) {  // P^T columns are free once dV_{i-1} is done
-        if (!mbar_wait(&bar[C::B_DVD], (i - 1) & 1, wc)) { ok = false; break; }
-        tc_fence_after();
-      }
-#pragma unroll
-      for (int c = 0; c < C::BQ / 32; ++c) tmem_st16(lane_base + C::COL_P + 16 * c, pp + 16 * c);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&bar[C::B_PF]);
-
-      if (i >= 1) {  // dS^T staging is free once dK_{i-1}, dQ_{i-1} are done
-        if (!mbar_wait(&bar[C::B_DSD], (i - 1) & 1, wc)) { ok = false; break; }
-      }
-#pragma unroll
-      for (int c = 0; c < C::BQ / 32; ++c) {
-        uint32_t dr[32];
-        tmem_ld32(lane_base + C::COL_DP + 32 * c, dr);
-        tmem_ld_wait();
-        reg_fence32(dr);
-        if (c == C::BQ / 32 - 1) {  // S^T and dP^T fully read
-          tc_fence_before();
-          mbar_arrive(&bar[C::B_SFREE]);
+        if (i >= 1) {  // P^T columns are free once dV_{i-1} is done
+          if (!warp_wait(&bar[C::B_DVD], (i - 1) & 1, wc)) { ok = false; break; }
+          tc_fence_after();
         }
+        tmem_st16(lane_base + C::COL_P + c0 / 2, pp);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bar[C::B_PF]);
         uint32_t w[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const int q = 32 * c + e;
-          const uint32_t pv = pp[16 * c + e / 2];
-          const float ds0 = bf16_lo(pv) * (__uint_as_float(dr[e]) - dd[q]);
-          const float ds1 = bf16_hi(pv) * (__uint_as_float(dr[e + 1]) - dd[q + 1]);
-          w[e / 2] = pack_bf16(ds0, ds1);
+          const float2 d2 = *reinterpret_cast<const float2*>(dd + e);
+          const uint32_t pv = pp[e / 2];
+          w[e / 2] = pack_bf16(bf16_lo(pv) * (__uint_as_float(dr[e]) - d2.x),
+                               bf16_hi(pv) * (__uint_as_float(dr[e + 1]) - d2.y));
         }
-        // Row krow of dS^T, queries [32c, 32c+32): four 16-byte chunks in the
-        // 128-byte-swizzled layout (chunk index XOR row % 8).
-        const uint32_t rowbase = sDS + (c >> 1) * C::DS_CHUNK + krow * 128;
+        if (i >= 1) {  // dS^T staging is free once dK_{i-1}, dQ_{i-1} are done
+          if (!warp_wait(&bar[C::B_DSD], (i - 1) & 1, wc)) { ok = false; break; }
+        }
+        // Row krow of dS^T, queries [c0, c0 + 32): four 16-byte chunks of the
+        // 128-byte row in the swizzled layout (chunk index XOR row % 8).
+        const uint32_t rowbase = sDS + krow * 128;
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const uint32_t chunk = (uint32_t)(((c & 1) * 4 + t) ^ (krow & 7));
-          st_shared_v4(rowbase + chunk * 16, w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
+        for (int t = 0; t < 4; ++t)
+          st_shared_v4(rowbase + (uint32_t)(((c0 / 8 + t) ^ (krow & 7)) * 16), w[4 * t],
+                       w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
+      } else {
+        // 64 columns per group, in chunks of 32 (registers do not hold both
+        // S^T and dP^T at once); S^T / dP^T are released after the last chunk.
+#pragma unroll
+        for (int c = 0; c < C::CW / 32; ++c) {
+          uint32_t sr[32];
+          tmem_ld32(lane_base + C::COL_S + c0 + 32 * c, sr);
+          tmem_ld_wait();
+          reg_fence32(sr);
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const int q = 32 * c + e;
+            const float2 l2 = *reinterpret_cast<const float2*>(lse + q);
+            float p0 = ex2(fmaf(__uint_as_float(sr[e]), sl2, -l2.x));
+            float p1 = ex2(fmaf(__uint_as_float(sr[e + 1]), sl2, -l2.y));
+            if (need_mask) {
+              if (q < qlim) p0 = 0.f;
+              if (q + 1 < qlim) p1 = 0.f;
+            }
+            if (!key_ok) p0 = p1 = 0.f;
+            pp[16 * c + e / 2] = pack_bf16(p0, p1);
+          }
+        }
+        if (i >= 1) {
+          if (!warp_wait(&bar[C::B_DVD], (i - 1) & 1, wc)) { ok = false; break; }
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int c = 0; c < C::CW / 32; ++c)
+          tmem_st16(lane_base + C::COL_P + c0 / 2 + 16 * c, pp + 16 * c);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bar[C::B_PF]);
+        if (i >= 1) {
+          if (!warp_wait(&bar[C::B_DSD], (i - 1) & 1, wc)) { ok = false; break; }
+        }
+#pragma unroll
+        for (int c = 0; c < C::CW / 32; ++c) {
+          uint32_t dr[32];
+          tmem_ld32(lane_base + C::COL_DP + c0 + 32 * c, dr);
+          tmem_ld_wait();
+          reg_fence32(dr);
+          if (c == C::CW / 32 - 1) {  // this group's S^T and dP^T fully read
+            tc_fence_before();
+            mbar_arrive(&bar[C::B_SFREE]);
+          }
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const int q = 32 * c + e;
+            const float2 d2 = *reinterpret_cast<const float2*>(dd + q);
+            const uint32_t pv = pp[16 * c + e / 2];
+            w[e / 2] = pack_bf16(bf16_lo(pv) * (__uint_as_float(dr[e]) - d2.x),
+                                 bf16_hi(pv) * (__uint_as_float(dr[e + 1]) - d2.y));
+          }
+          // 64-query chunk (c0 + 32c) / 64 of dS^T, 16-byte chunks ((c0+32c) % 64) / 8 + t
+          const int qc = c0 + 32 * c;
+          const uint32_t rowbase = sDS + (qc >> 6) * C::DS_CHUNK + krow * 128;
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const uint32_t chunk = (uint32_t)((((qc & 63) >> 3) + t) ^ (krow & 7));
+            st_shared_v4(rowbase + chunk * 16, w[4 * t], w[4 * t + 1], w[4 * t + 2],
+                         w[4 * t + 3]);
+          }
         }
       }
       fence_proxy_async_smem();
@@ -366,25 +428,22 @@ __global__ void __launch_bounds__(384, 1)
     }
 
     // ------------------------------------------------------------ dK, dV out
+    // Group 0 writes dV, group 1 writes dK (each all D columns of its rows).
     if (ok) {
       __nv_bfloat16* dv_row = p.dV + ((size_t)bh * p.m + kg) * D;
       __nv_bfloat16* dk_row = p.dK + ((size_t)bh * p.m + kg) * D;
+      const uint32_t col = half == 0 ? C::COL_DV : C::COL_DK;
+      const float mul = half == 0 ? 1.f : p.scale;
+      __nv_bfloat16* dst_row = half == 0 ? dv_row : dk_row;
       if (nq == 0) {
         if (key_ok) {
           const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-          for (int c = 0; c < D / 8; ++c) {
-            reinterpret_cast<uint4*>(dv_row)[c] = z;
-            reinterpret_cast<uint4*>(dk_row)[c] = z;
-          }
+          for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(dst_row)[c] = z;
         }
-      } else if (mbar_wait(&bar[C::B_ACC], 0, wc)) {
+      } else if (warp_wait(&bar[C::B_ACC], 0, wc)) {
         tc_fence_after();
-#pragma unroll
-        for (int which = 0; which < 2; ++which) {
-          const uint32_t col = which == 0 ? C::COL_DV : C::COL_DK;
-          const float mul = which == 0 ? 1.f : p.scale;
-          __nv_bfloat16* dst_row = which == 0 ? dv_row : dk_row;
+        {
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
@@ -406,28 +465,47 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
     }
-  } else if (warp >= 8) {
+  } else if (warp >= 12) {
     // ------------------------------------------------------------ dQ drain
-    const int t = (warp - 8) * 32 + lane;  // TMEM lane
+    const int t = (warp - 12) * 32 + lane;  // TMEM lane
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    bool ok = true;
     for (int i = 0; i < nq; ++i) {
       const int q0 = (i_start + i) * C::BQ;
-      if (!mbar_wait(&bar[C::B_DSD], i & 1, wc)) break;
-      tc_fence_after();
+      // Every thread of the group takes every iteration (also after an abort) so
+      // that the named barriers below always see all 128 threads.
+      if (ok) ok = warp_wait(&bar[C::B_DSD], i & 1, wc);
       uint32_t v[64];
-      tmem_ld32(lane_base + C::COL_DQ, v);
-      tmem_ld32(lane_base + C::COL_DQ + 32, v + 32);
-      tmem_ld_wait();
-      reg_fence32(v);
-      reg_fence32(v + 32);
-      tc_fence_before();
-      mbar_arrive(&bar[C::B_DQE]);
+      if (ok) {
+        tc_fence_after();
+        tmem_ld32(lane_base + C::COL_DQ, v);
+        tmem_ld32(lane_base + C::COL_DQ + 32, v + 32);
+        tmem_ld_wait();
+        reg_fence32(v);
+        reg_fence32(v + 32);
+        tc_fence_before();
+        mbar_arrive(&bar[C::B_DQE]);
+      }
       if (D == 128) {
-        // lane t = feature index, column = query
-        float* base = p.ws_dQ + ((size_t)bh * p.n_pad + q0) * D + t;
+        // lane t = feature index, column = query. Stage the 64 x 128 fp32 block
+        // row-major in shared memory, then one thread adds it to the accumulator
+        // with a single 32 KB bulk reduction.
+        float* buf = reinterpret_cast<float*>(smem + C::OFF_DQS);
+        if (i >= 1) {
+          if (t == 0) bulk_wait_group_read<0>();  // the previous reduction has read buf
+          named_barrier(1, 128);
+        }
+        if (ok) {
 #pragma unroll
-        for (int q = 0; q < 64; ++q) atomicAdd(base + (size_t)q * D, __uint_as_float(v[q]));
-      } else {
+          for (int q = 0; q < 64; ++q) buf[q * D + t] = __uint_as_float(v[q]);
+        }
+        fence_proxy_async_smem();
+        named_barrier(1, 128);
+        if (t == 0 && ok) {
+          bulk_reduce_add_f32(p.ws_dQ + ((size_t)bh * p.n_pad + q0) * D, buf, C::DQS_BYTES);
+          bulk_commit_group();
+        }
+      } else if (ok) {
         // lane t = query, column = feature index
         float4* base = reinterpret_cast<float4*>(p.ws_dQ + ((size_t)bh * p.n_pad + q0 + t) * D);
 #pragma unroll
@@ -437,6 +515,7 @@ __global__ void __launch_bounds__(384, 1)
                                           __uint_as_float(v[4 * c + 3])));
       }
     }
+    if (D == 128 && t == 0) bulk_wait_group_all();  // reductions complete before exit
   }
 
   tc_fence_before();
@@ -538,10 +617,12 @@ cudaError_t launch_dkdv_d(const BwdArgs& a, cudaStream_t stream) {
   p.causal = a.causal;
   p.scale = a.scale;
   p.scale_log2 = a.scale * kLog2e;
+  p.ktiles = ceil_div(a.m, C::BN);
+  p.group = heads_per_group(a.BH, p.ktiles);
   cudaError_t e =
       cudaFuncSetAttribute(dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  const unsigned grid = (unsigned)ceil_div(a.m, C::BN) * (unsigned)a.BH;
+  const unsigned grid = (unsigned)p.ktiles * (unsigned)a.BH;
   dkdv_kernel<D><<<grid, C::THREADS, C::SMEM, stream>>>(mq, mk, mv, mdo, ml2, md, p);
   return cudaGetLastError();
 }

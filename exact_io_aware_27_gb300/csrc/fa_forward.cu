@@ -64,7 +64,7 @@ struct FwdCfg {
 struct FwdParams {
   __nv_bfloat16* O;
   float* L;
-  int n, m, BH, causal, num_q_tiles;
+  int n, m, BH, causal, num_q_tiles, group;
   float scale_log2;  // scale * log2(e)
 };
 
@@ -91,9 +91,10 @@ __global__ void __launch_bounds__(256, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // Tile-major block order: every head's heaviest tiles are scheduled first.
-  int tile = blockIdx.x / p.BH;
-  const int bh = blockIdx.x % p.BH;
+  // Heads a group at a time (their K/V stay in L2 while the group runs); inside
+  // a group the heaviest tiles (the last ones, under causal masking) go first.
+  int tile, bh;
+  grouped_tile(blockIdx.x, p.BH, p.num_q_tiles, p.group, tile, bh);
   if (p.causal) tile = p.num_q_tiles - 1 - tile;
   const int qs = tile * C::BM;
   int nkb = (p.m + C::BN - 1) / C::BN;
@@ -222,7 +223,7 @@ __global__ void __launch_bounds__(256, 1)
     bool ok = true;
     for (int j = 0; j < nkb; ++j) {
       const int sb = j & 1;
-      if (!mbar_wait(&bar[C::B_SF + sb], (j >> 1) & 1, wc)) {
+      if (!warp_wait(&bar[C::B_SF + sb], (j >> 1) & 1, wc)) {
         ok = false;
         break;
       }
@@ -272,7 +273,7 @@ __global__ void __launch_bounds__(256, 1)
 
       // P buffer sb and the O accumulator are free once P_{j-1} V_{j-1} is done.
       if (j >= 1) {
-        if (!mbar_wait(&bar[C::B_OD], (j - 1) & 1, wc)) {
+        if (!warp_wait(&bar[C::B_OD], (j - 1) & 1, wc)) {
           ok = false;
           break;
         }
@@ -299,7 +300,7 @@ __global__ void __launch_bounds__(256, 1)
     }
 
     // ------------------------------------------------------------ epilogue
-    if (ok && mbar_wait(&bar[C::B_OD], (nkb - 1) & 1, wc)) {
+    if (ok && warp_wait(&bar[C::B_OD], (nkb - 1) & 1, wc)) {
       tc_fence_after();
       const float inv_l = 1.f / l_run;
       __nv_bfloat16* orow = p.O + ((size_t)bh * p.n + qg) * D;
@@ -349,6 +350,7 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
   p.BH = a.BH;
   p.causal = a.causal;
   p.num_q_tiles = ceil_div(a.n, C::BM);
+  p.group = heads_per_group(a.BH, p.num_q_tiles);
   p.scale_log2 = a.scale * 1.44269504088896340736f;
   cudaError_t e =
       cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);

@@ -16,6 +16,10 @@ constexpr int kWorkspaceRowAlign = 128;
 inline int round_up(int x, int a) { return (x + a - 1) / a * a; }
 inline int ceil_div(int x, int a) { return (x + a - 1) / a; }
 
+// Heads per launch-order group (see grouped_tile): enough blocks for about two
+// waves over the SMs, so the blocks in flight touch few heads.
+int heads_per_group(int BH, int tiles_per_head);
+
 // cuTensorMapEncodeTiled, fetched from the driver at first use.
 CUresult encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, cuuint32_t rank,
                            void* base, const cuuint64_t* dims, const cuuint64_t* strides_bytes,

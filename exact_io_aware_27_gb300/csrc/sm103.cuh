@@ -75,6 +75,26 @@ FA_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
   return false;
 }
 
+// mbar_wait for a whole warp: every lane polls, and the result is agreed
+// across the warp so that warp-collective instructions (tcgen05.ld/st) that
+// follow are reached by all lanes or by none.
+FA_DEV bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, w));
+}
+
+// Linear block index -> (tile rank within a head, head). Heads are taken in
+// groups of `group`; inside a group, rank 0 of every head comes first, then
+// rank 1, and so on, so that the blocks in flight share a few heads' data in L2.
+FA_DEV void grouped_tile(int lin, int BH, int tiles, int group, int& rank, int& bh) {
+  const int per_group = group * tiles;
+  const int g = lin / per_group;
+  const int base = g * group;
+  const int gsize = min(group, BH - base);
+  const int r = lin - g * per_group;
+  rank = r / gsize;
+  bh = base + r % gsize;
+}
+
 // ---------------------------------------------------------------- TMA
 FA_DEV void tma_prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -100,6 +120,29 @@ FA_DEV void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0
 // proxy (tensor-core operand reads).
 FA_DEV void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Bulk (non-tensor) reduction: global[dst .. dst+bytes) += shared[src ..] as
+// fp32, issued by one thread; both addresses 16-byte aligned, bytes a multiple
+// of 16. Tracked by the issuing thread's bulk async-group.
+FA_DEV void bulk_reduce_add_f32(float* gdst, const void* ssrc, uint32_t bytes) {
+  asm volatile(
+      "cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(gdst),
+      "r"(smem_u32(ssrc)), "r"(bytes)
+      : "memory");
+}
+FA_DEV void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until at most N of this thread's bulk groups still read shared memory.
+template <int N>
+FA_DEV void bulk_wait_group_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Waits until all of this thread's bulk groups have completed (writes visible).
+FA_DEV void bulk_wait_group_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Named barrier over `count` threads (a multiple of 32); id 0 is __syncthreads.
+FA_DEV void named_barrier(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05
