@@ -202,86 +202,87 @@ __global__ void __launch_bounds__(512, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && nq > 0) {
+    // The whole warp runs this loop (operands stay warp-uniform); elect.sync
+    // picks the lane that issues each tcgen05 instruction. Descriptors are built
+    // once per operand buffer and advanced by compile-time byte offsets.
+    if (nq > 0) {
       constexpr uint32_t kIdescS = idesc_bf16_f32(128, C::BQ, false, false);
       constexpr uint32_t kIdescDV = idesc_bf16_f32(128, D, false, true);
       constexpr uint32_t kIdescDK = idesc_bf16_f32(128, D, false, true);
       constexpr uint32_t kIdescDQ = (D == 128) ? idesc_bf16_f32(128, C::BQ, true, true)
                                                : idesc_bf16_f32(128, D, true, true);
-      const uint32_t sK = smem_u32(smem + C::OFF_K);
-      const uint32_t sV = smem_u32(smem + C::OFF_V);
-      const uint32_t sDS = smem_u32(smem + C::OFF_DS);
-      bool ok = mbar_wait(&bar[C::B_KV], 0, wc);
+      const uint64_t dK_k = sdesc_sw128(smem_u32(smem + C::OFF_K), 16, 1024);  // K, K-major
+      const uint64_t dV_k = sdesc_sw128(smem_u32(smem + C::OFF_V), 16, 1024);  // V, K-major
+      const uint64_t dK_mn = sdesc_sw128(smem_u32(smem + C::OFF_K), C::KV_CHUNK, 1024);
+      const uint64_t dS_k = sdesc_sw128(smem_u32(smem + C::OFF_DS), 16, 1024);   // dS^T rows
+      const uint64_t dS_mn = sdesc_sw128(smem_u32(smem + C::OFF_DS), C::DS_CHUNK, 1024);
+      bool ok = warp_wait(&bar[C::B_KV], 0, wc);
       for (int i = 0; ok && i <= nq; ++i) {
         if (i < nq) {
           // S^T = K Q_i^T and dP^T = V dO_i^T, as soon as block i-1's are read
           const int s = i % C::STAGES;
           const uint32_t ph = (i / C::STAGES) & 1;
-          if (!mbar_wait(&bar[C::B_QF + s], ph, wc)) break;
-          if (!mbar_wait(&bar[C::B_OF + s], ph, wc)) break;
-          if (i >= 1 && !mbar_wait(&bar[C::B_SFREE], (i - 1) & 1, wc)) break;
+          if (!warp_wait(&bar[C::B_QF + s], ph, wc)) break;
+          if (!warp_wait(&bar[C::B_OF + s], ph, wc)) break;
+          if (i >= 1 && !warp_wait(&bar[C::B_SFREE], (i - 1) & 1, wc)) break;
           tc_fence_after();
-          const uint32_t sQ = smem_u32(smem + C::OFF_Q + s * C::Q_TILE);
-          const uint32_t sO = smem_u32(smem + C::OFF_DO + s * C::Q_TILE);
+          const uint64_t dQ_k = sdesc_sw128(smem_u32(smem + C::OFF_Q + s * C::Q_TILE), 16, 1024);
+          const uint64_t dO_k = sdesc_sw128(smem_u32(smem + C::OFF_DO + s * C::Q_TILE), 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t ka = (kk >> 2) * C::KV_CHUNK + (kk & 3) * 32;
             const uint32_t kb = (kk >> 2) * C::Q_CHUNK + (kk & 3) * 32;
-            umma_ss(tmem + C::COL_S, sdesc_sw128(sK + ka, 16, 1024),
-                    sdesc_sw128(sQ + kb, 16, 1024), kIdescS, kk > 0);
+            umma_ss_w(tmem + C::COL_S, sdesc_add(dK_k, ka), sdesc_add(dQ_k, kb), kIdescS, kk > 0);
           }
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t ka = (kk >> 2) * C::KV_CHUNK + (kk & 3) * 32;
             const uint32_t kb = (kk >> 2) * C::Q_CHUNK + (kk & 3) * 32;
-            umma_ss(tmem + C::COL_DP, sdesc_sw128(sV + ka, 16, 1024),
-                    sdesc_sw128(sO + kb, 16, 1024), kIdescS, kk > 0);
+            umma_ss_w(tmem + C::COL_DP, sdesc_add(dV_k, ka), sdesc_add(dO_k, kb), kIdescS, kk > 0);
           }
-          umma_commit(&bar[C::B_SF]);
+          umma_commit_w(&bar[C::B_SF]);
         }
         if (i >= 1) {
           const int ii = i - 1;
           const int s = ii % C::STAGES;
           // dV += P^T dO_{i-1}
-          if (!mbar_wait(&bar[C::B_PF], ii & 1, wc)) break;
+          if (!warp_wait(&bar[C::B_PF], ii & 1, wc)) break;
           tc_fence_after();
-          const uint32_t sO = smem_u32(smem + C::OFF_DO + s * C::Q_TILE);
+          const uint64_t dO_mn =
+              sdesc_sw128(smem_u32(smem + C::OFF_DO + s * C::Q_TILE), C::Q_CHUNK, 1024);
 #pragma unroll
-          for (int kk = 0; kk < C::BQ / 16; ++kk) {
-            umma_ts(tmem + C::COL_DV, tmem + C::COL_P + kk * 8,
-                    sdesc_sw128(sO + kk * 2048, C::Q_CHUNK, 1024), kIdescDV,
-                    (ii > 0 || kk > 0) ? 1u : 0u);
-          }
-          umma_commit(&bar[C::B_DVD]);
-          umma_commit(&bar[C::B_OE + s]);
+          for (int kk = 0; kk < C::BQ / 16; ++kk)
+            umma_ts_w(tmem + C::COL_DV, tmem + C::COL_P + kk * 8, sdesc_add(dO_mn, kk * 2048),
+                      kIdescDV, (ii > 0 || kk > 0) ? 1u : 0u);
+          umma_commit_w(&bar[C::B_DVD]);
+          umma_commit_w(&bar[C::B_OE + s]);
           // dK += dS^T Q_{i-1} and this block's share of dQ_{i-1}
-          if (!mbar_wait(&bar[C::B_DSF], ii & 1, wc)) break;
-          if (ii >= 1 && !mbar_wait(&bar[C::B_DQE], (ii - 1) & 1, wc)) break;
+          if (!warp_wait(&bar[C::B_DSF], ii & 1, wc)) break;
+          if (ii >= 1 && !warp_wait(&bar[C::B_DQE], (ii - 1) & 1, wc)) break;
           tc_fence_after();
-          const uint32_t sQ = smem_u32(smem + C::OFF_Q + s * C::Q_TILE);
+          const uint64_t dQ_mn =
+              sdesc_sw128(smem_u32(smem + C::OFF_Q + s * C::Q_TILE), C::Q_CHUNK, 1024);
 #pragma unroll
           for (int kk = 0; kk < C::BQ / 16; ++kk) {
             const uint32_t ka = (kk >> 2) * C::DS_CHUNK + (kk & 3) * 32;
-            umma_ss(tmem + C::COL_DK, sdesc_sw128(sDS + ka, 16, 1024),
-                    sdesc_sw128(sQ + kk * 2048, C::Q_CHUNK, 1024), kIdescDK,
-                    (ii > 0 || kk > 0) ? 1u : 0u);
+            umma_ss_w(tmem + C::COL_DK, sdesc_add(dS_k, ka), sdesc_add(dQ_mn, kk * 2048), kIdescDK,
+                      (ii > 0 || kk > 0) ? 1u : 0u);
           }
 #pragma unroll
           for (int kk = 0; kk < C::BN / 16; ++kk) {
-            if (D == 128) {
-              umma_ss(tmem + C::COL_DQ, sdesc_sw128(sK + kk * 2048, C::KV_CHUNK, 1024),
-                      sdesc_sw128(sDS + kk * 2048, C::DS_CHUNK, 1024), kIdescDQ, kk > 0);
-            } else {
-              umma_ss(tmem + C::COL_DQ, sdesc_sw128(sDS + kk * 2048, C::DS_CHUNK, 1024),
-                      sdesc_sw128(sK + kk * 2048, C::KV_CHUNK, 1024), kIdescDQ, kk > 0);
-            }
+            if (D == 128)
+              umma_ss_w(tmem + C::COL_DQ, sdesc_add(dK_mn, kk * 2048), sdesc_add(dS_mn, kk * 2048),
+                        kIdescDQ, kk > 0);
+            else
+              umma_ss_w(tmem + C::COL_DQ, sdesc_add(dS_mn, kk * 2048), sdesc_add(dK_mn, kk * 2048),
+                        kIdescDQ, kk > 0);
           }
-          umma_commit(&bar[C::B_DSD]);
-          umma_commit(&bar[C::B_QE + s]);
+          umma_commit_w(&bar[C::B_DSD]);
+          umma_commit_w(&bar[C::B_QE + s]);
         }
       }
-      umma_commit(&bar[C::B_ACC]);
-      umma_commit(&bar[C::B_DRAIN]);
+      umma_commit_w(&bar[C::B_ACC]);
+      umma_commit_w(&bar[C::B_DRAIN]);
       drain_wait(&bar[C::B_DRAIN], 0);
     }
   } else if (warp >= 4 && warp < 12) {

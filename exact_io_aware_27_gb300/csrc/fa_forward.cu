@@ -167,49 +167,51 @@ __global__ void __launch_bounds__(256, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the loop (operands stay warp-uniform); elect.sync picks
+    // the issuing lane. Descriptors are built once per buffer and advanced by
+    // compile-time byte offsets.
+    {
       constexpr uint32_t kIdescS = idesc_bf16_f32(128, C::BN, false, false);
       constexpr uint32_t kIdescO = idesc_bf16_f32(128, D, false, true);
-      const uint32_t sQ = smem_u32(smem + C::OFF_Q);
-      bool ok = mbar_wait(&bar[C::B_Q], 0, wc);
+      const uint64_t dQ_k = sdesc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024);
+      bool ok = warp_wait(&bar[C::B_Q], 0, wc);
       for (int j = 0; ok && j <= nkb; ++j) {
         if (j < nkb) {
           const int s = j % C::STAGES;
           const int sb = j & 1;
-          if (!mbar_wait(&bar[C::B_KF + s], (j / C::STAGES) & 1, wc)) break;
+          if (!warp_wait(&bar[C::B_KF + s], (j / C::STAGES) & 1, wc)) break;
           // S buffer sb was last read by the softmax of block j - 2.
-          if (j >= 2 && !mbar_wait(&bar[C::B_PF + sb], ((j - 2) >> 1) & 1, wc)) break;
+          if (j >= 2 && !warp_wait(&bar[C::B_PF + sb], ((j - 2) >> 1) & 1, wc)) break;
           tc_fence_after();
-          const uint32_t sK = smem_u32(smem + C::OFF_K + s * C::TILE);
+          const uint64_t dK_k = sdesc_sw128(smem_u32(smem + C::OFF_K + s * C::TILE), 16, 1024);
           const uint32_t dS = tmem + (sb ? C::COL_S1 : C::COL_S0);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
-            umma_ss(dS, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024),
-                    kIdescS, kk > 0);
+            umma_ss_w(dS, sdesc_add(dQ_k, off), sdesc_add(dK_k, off), kIdescS, kk > 0);
           }
-          umma_commit(&bar[C::B_SF + sb]);
-          umma_commit(&bar[C::B_KE + s]);
+          umma_commit_w(&bar[C::B_SF + sb]);
+          umma_commit_w(&bar[C::B_KE + s]);
         }
         if (j >= 1) {
           const int jj = j - 1;
           const int s = jj % C::STAGES;
           const int pb = jj & 1;
-          if (!mbar_wait(&bar[C::B_PF + pb], (jj >> 1) & 1, wc)) break;
-          if (!mbar_wait(&bar[C::B_VF + s], (jj / C::STAGES) & 1, wc)) break;
+          if (!warp_wait(&bar[C::B_PF + pb], (jj >> 1) & 1, wc)) break;
+          if (!warp_wait(&bar[C::B_VF + s], (jj / C::STAGES) & 1, wc)) break;
           tc_fence_after();
-          const uint32_t sV = smem_u32(smem + C::OFF_V + s * C::TILE);
+          const uint64_t dV_mn =
+              sdesc_sw128(smem_u32(smem + C::OFF_V + s * C::TILE), C::CHUNK, 1024);
           const uint32_t aP = tmem + (pb ? C::COL_P1 : C::COL_P0);
 #pragma unroll
-          for (int kk = 0; kk < C::BN / 16; ++kk) {
-            umma_ts(tmem + C::COL_O, aP + kk * 8, sdesc_sw128(sV + kk * 2048, C::CHUNK, 1024),
-                    kIdescO, (jj > 0 || kk > 0) ? 1u : 0u);
-          }
-          umma_commit(&bar[C::B_OD]);
-          umma_commit(&bar[C::B_VE + s]);
+          for (int kk = 0; kk < C::BN / 16; ++kk)
+            umma_ts_w(tmem + C::COL_O, aP + kk * 8, sdesc_add(dV_mn, kk * 2048), kIdescO,
+                      (jj > 0 || kk > 0) ? 1u : 0u);
+          umma_commit_w(&bar[C::B_OD]);
+          umma_commit_w(&bar[C::B_VE + s]);
         }
       }
-      umma_commit(&bar[C::B_DRAIN]);
+      umma_commit_w(&bar[C::B_DRAIN]);
       drain_wait(&bar[C::B_DRAIN], 0);
     }
   } else if (warp >= 4) {
