@@ -50,6 +50,12 @@ struct BwdCfg {
   static constexpr int DS_CHUNK = BN * 128;         // 64 queries x 128 keys of dS^T (bf16)
   static constexpr int DS_TILE = (BQ / 64) * DS_CHUNK;
   static constexpr int STAGES = 3;
+  // dK reads dS^T from TMEM (the TS form) instead of shared memory; needs BQ/2
+  // spare TMEM columns, which only the d = 128 layout has.
+  static constexpr bool kDsInTmem = (D == 128);
+  // dQ partials staged in shared memory and added with one bulk reduction per
+  // block (true), or added straight from registers with fp32 reductions (false).
+  static constexpr bool kDqStaged = false;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + KV_TILE;
   static constexpr int OFF_Q = OFF_V + KV_TILE;
@@ -58,7 +64,7 @@ struct BwdCfg {
   static constexpr int OFF_LSE = OFF_DS + DS_TILE;          // [STAGES][BQ] fp32
   static constexpr int OFF_DD = OFF_LSE + STAGES * BQ * 4;  // [STAGES][BQ] fp32
   static constexpr int OFF_DQS = OFF_DD + STAGES * BQ * 4;  // [BQ x D] fp32 dQ staging
-  static constexpr int DQS_BYTES = (D == 128) ? BQ * D * 4 : 0;
+  static constexpr int DQS_BYTES = (D == 128 && kDqStaged) ? BQ * D * 4 : 0;
   static constexpr int OFF_BAR = OFF_DQS + DQS_BYTES;
   // barrier slots
   static constexpr int B_KV = 0;
@@ -84,10 +90,11 @@ struct BwdCfg {
   static constexpr uint32_t COL_DV = 2 * BQ + BQ / 2;
   static constexpr uint32_t COL_DK = COL_DV + D;
   static constexpr uint32_t COL_DQ = COL_DK + D;
+  static constexpr uint32_t COL_DST = COL_DQ + 64;  // dS^T as bf16 pairs (kDsInTmem)
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr int THREADS = 512;
   static constexpr int COMPUTE_THREADS = 256;
-  static_assert(COL_DQ + 64 <= TMEM_COLS, "TMEM budget");
+  static_assert(COL_DST + (kDsInTmem ? BQ / 2 : 0) <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
@@ -265,8 +272,12 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
           for (int kk = 0; kk < C::BQ / 16; ++kk) {
             const uint32_t ka = (kk >> 2) * C::DS_CHUNK + (kk & 3) * 32;
-            umma_ss_w(tmem + C::COL_DK, sdesc_add(dS_k, ka), sdesc_add(dQ_mn, kk * 2048), kIdescDK,
-                      (ii > 0 || kk > 0) ? 1u : 0u);
+            if (C::kDsInTmem)
+              umma_ts_w(tmem + C::COL_DK, tmem + C::COL_DST + kk * 8, sdesc_add(dQ_mn, kk * 2048),
+                        kIdescDK, (ii > 0 || kk > 0) ? 1u : 0u);
+            else
+              umma_ss_w(tmem + C::COL_DK, sdesc_add(dS_k, ka), sdesc_add(dQ_mn, kk * 2048),
+                        kIdescDK, (ii > 0 || kk > 0) ? 1u : 0u);
           }
 #pragma unroll
           for (int kk = 0; kk < C::BN / 16; ++kk) {
@@ -351,6 +362,7 @@ __global__ void __launch_bounds__(512, 1)
         if (i >= 1) {  // dS^T staging is free once dK_{i-1}, dQ_{i-1} are done
           if (!warp_wait(&bar[C::B_DSD], (i - 1) & 1, wc)) { ok = false; break; }
         }
+        if (C::kDsInTmem) tmem_st16(lane_base + C::COL_DST + c0 / 2, w);
         // Row krow of dS^T, queries [c0, c0 + 32): four 16-byte chunks of the
         // 128-byte row in the swizzled layout (chunk index XOR row % 8).
         const uint32_t rowbase = sDS + krow * 128;
@@ -358,6 +370,10 @@ __global__ void __launch_bounds__(512, 1)
         for (int t = 0; t < 4; ++t)
           st_shared_v4(rowbase + (uint32_t)(((c0 / 8 + t) ^ (krow & 7)) * 16), w[4 * t],
                        w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
+        if (C::kDsInTmem) {
+          tmem_st_wait();
+          tc_fence_before();
+        }
       } else {
         // 64 columns per group, in chunks of 32 (registers do not hold both
         // S^T and dP^T at once); S^T / dP^T are released after the last chunk.
@@ -487,7 +503,7 @@ __global__ void __launch_bounds__(512, 1)
         tc_fence_before();
         mbar_arrive(&bar[C::B_DQE]);
       }
-      if (D == 128) {
+      if (D == 128 && C::kDqStaged) {
         // lane t = feature index, column = query. Stage the 64 x 128 fp32 block
         // row-major in shared memory, then one thread adds it to the accumulator
         // with a single 32 KB bulk reduction.
@@ -506,6 +522,12 @@ __global__ void __launch_bounds__(512, 1)
           bulk_reduce_add_f32(p.ws_dQ + ((size_t)bh * p.n_pad + q0) * D, buf, C::DQS_BYTES);
           bulk_commit_group();
         }
+      } else if (D == 128 && ok) {
+        // lane t = feature index, column = query: each warp adds 32 consecutive
+        // floats of one accumulator row per instruction.
+        float* base = p.ws_dQ + ((size_t)bh * p.n_pad + q0) * D + t;
+#pragma unroll
+        for (int q = 0; q < 64; ++q) atomicAdd(base + (size_t)q * D, __uint_as_float(v[q]));
       } else if (ok) {
         // lane t = query, column = feature index
         float4* base = reinterpret_cast<float4*>(p.ws_dQ + ((size_t)bh * p.n_pad + q0 + t) * D);
@@ -516,7 +538,7 @@ __global__ void __launch_bounds__(512, 1)
                                           __uint_as_float(v[4 * c + 3])));
       }
     }
-    if (D == 128 && t == 0) bulk_wait_group_all();  // reductions complete before exit
+    if (D == 128 && C::kDqStaged && t == 0) bulk_wait_group_all();  // reductions done before exit
   }
 
   tc_fence_before();
