@@ -1,24 +1,33 @@
 // Forward pass of exact attention: O = softmax(Q K^T * scale) V and the
-// natural-log logsumexp L, one 128-row query tile per CTA.
+// natural-log logsumexp L, two 128-row query tiles per CTA.
 //
 // Method: "05_flash_attention.py", flash_attention_forward. For each query
 // tile the key/value blocks are visited left to right; per row the kernel
-// keeps the running maximum m and the rescaled exponential sum l, forms
-// P = exp(S - m_new), rescales the output accumulator by exp(m_old - m_new)
-// and adds P V. At the end O = O / l and L = m + log l. Under causal masking
-// key blocks wholly to the right of the tile's last query are never visited,
-// and the diagonal block masks k > q.
+// keeps a reference maximum m and the exponential sum l taken relative to it,
+// forms P = exp(S - m), and adds P V to the output accumulator; whenever m
+// moves, O and l are rescaled by exp(m_old - m_new). At the end O = O / l and
+// L = m + log l. Under causal masking key blocks wholly to the right of a
+// tile's last query are never visited, and the diagonal block masks k > q.
+// The reference maximum is moved only when a row maximum exceeds it by more
+// than 8 (base 2): until then P stays below 2^8 and O, l keep their common
+// reference, so the result is the same up to rounding while most blocks need
+// no rescaling of O.
 //
-// GB300 mapping (one CTA per (query tile, head), 256 threads):
-//   warp 0      TMA producer: Q once, then K_j and V_j into a STAGES-deep ring
-//   warp 1      MMA issuer: S_j = Q K_j^T (SS form) into TMEM buffer j % 2,
-//               then O += P_{j-1} V_{j-1} (TS form, P read from TMEM)
-//   warps 4..7  softmax: thread r owns query row r (= TMEM lane r); reads S
-//               with tcgen05.ld, masks, updates (m, l) in base 2 (exp2 via
-//               ex2.approx), writes P as bf16 into TMEM, rescales the O row
-//               when its maximum moved, and runs the epilogue.
-// TMEM (512 columns): S0 [0,128) S1 [128,256) P0 [256,320) P1 [320,384)
-// O [384, 384+d). Scores, probabilities and the accumulator never leave the SM.
+// GB300 mapping (one CTA per (pair of query tiles, head), 384 threads):
+//   warp 0       TMA producer: Q of both tiles once, then K_j and V_j into a
+//                STAGES-deep ring shared by the two tiles
+//   warp 1       MMA issuer (whole warp, one elected lane issues):
+//                S0 = Q0 K_j^T, S1 = Q1 K_j^T, then O0 += P0 V_j, O1 += P1 V_j
+//                (P read from TMEM); S_t of block j+1 waits for O_t += P_t V_j
+//   warps 4..7   softmax of tile 0, warps 8..11 softmax of tile 1: thread r
+//                owns query row r of its tile (= TMEM lane r); reads the S row
+//                with tcgen05.ld, masks, updates (m, l) in base 2 (exp2 via
+//                ex2.approx), writes P as bf16 over the first 64 columns of
+//                its own S row, rescales its O row when m moved, and runs the
+//                epilogue. While one tile's softmax runs, the tensor cores work
+//                on the other tile.
+// TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256, 256+d) O1 [256+d, 256+2d).
+// Scores, probabilities and the accumulators never leave the SM.
 #include "fa_internal.h"
 #include "sm103.cuh"
 
@@ -29,17 +38,19 @@ __device__ unsigned int g_fwd_status;
 namespace {
 
 constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kRescaleThreshold = 8.0f;  // base-2 units: P stays below 2^8
 
 template <int D>
 struct FwdCfg {
-  static constexpr int BM = 128;                 // query rows per CTA = TMEM lanes
+  static constexpr int BM = 128;                 // query rows per tile = TMEM lanes
+  static constexpr int TILES = 2;                // query tiles per CTA
   static constexpr int BN = 128;                 // keys per block
   static constexpr int KCH = D / 64;             // 128-byte column chunks per row
   static constexpr int CHUNK = 128 * 128;        // bytes of one chunk of a 128-row tile
   static constexpr int TILE = KCH * CHUNK;       // bytes of a Q, K or V tile
   static constexpr int STAGES = (D == 128) ? 2 : 4;
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + TILE;
+  static constexpr int OFF_Q = 0;                // TILES query tiles
+  static constexpr int OFF_K = OFF_Q + TILES * TILE;
   static constexpr int OFF_V = OFF_K + STAGES * TILE;
   static constexpr int OFF_BAR = OFF_V + STAGES * TILE;
   // barrier slots
@@ -48,23 +59,24 @@ struct FwdCfg {
   static constexpr int B_KE = B_KF + STAGES;
   static constexpr int B_VF = B_KE + STAGES;
   static constexpr int B_VE = B_VF + STAGES;
-  static constexpr int B_SF = B_VE + STAGES;  // 2
-  static constexpr int B_PF = B_SF + 2;       // 2
-  static constexpr int B_OD = B_PF + 2;
-  static constexpr int B_DRAIN = B_OD + 1;
+  static constexpr int B_SF = B_VE + STAGES;    // + tile: S_t ready
+  static constexpr int B_PF = B_SF + TILES;     // + tile: P_t written, O_t rescaled
+  static constexpr int B_PVD = B_PF + TILES;    // + tile: O_t += P_t V done
+  static constexpr int B_DRAIN = B_PVD + TILES;
   static constexpr int NBAR = B_DRAIN + 1;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;
-  static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_P0 = 256, COL_P1 = 320,
-                            COL_O = 384, TMEM_COLS = 512;
-  static constexpr int THREADS = 256;
-  static_assert(COL_O + D <= TMEM_COLS, "TMEM budget");
+  static constexpr uint32_t COL_S = 0;           // + 128 * tile
+  static constexpr uint32_t COL_O = 256;         // + D * tile
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr int THREADS = 384;
+  static_assert(COL_O + TILES * D <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
 struct FwdParams {
   __nv_bfloat16* O;
   float* L;
-  int n, m, BH, causal, num_q_tiles, group;
+  int n, m, BH, causal, num_pairs, group;
   float scale_log2;  // scale * log2(e)
 };
 
@@ -77,8 +89,16 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// Key blocks a tile of rows [q0, q0 + 128) visits (0 if the tile is past n).
+__device__ __forceinline__ int tile_blocks(int q0, int n, int m, int causal) {
+  if (q0 >= n) return 0;
+  int nkb = (m + 127) / 128;
+  if (causal) nkb = min(nkb, (min(q0 + 127, n - 1)) / 128 + 1);  // keys k <= q
+  return nkb;
+}
+
 template <int D>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
   using C = FwdCfg<D>;
@@ -92,16 +112,14 @@ __global__ void __launch_bounds__(256, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   // Heads a group at a time (their K/V stay in L2 while the group runs); inside
-  // a group the heaviest tiles (the last ones, under causal masking) go first.
-  int tile, bh;
-  grouped_tile(blockIdx.x, p.BH, p.num_q_tiles, p.group, tile, bh);
-  if (p.causal) tile = p.num_q_tiles - 1 - tile;
-  const int qs = tile * C::BM;
-  int nkb = (p.m + C::BN - 1) / C::BN;
-  if (p.causal) {
-    const int qmax = min(qs + C::BM, p.n) - 1;  // top-left mask: keys k <= q
-    nkb = min(nkb, qmax / C::BN + 1);
-  }
+  // a group the heaviest tile pairs (the last ones, under causal masking) go first.
+  int pair, bh;
+  grouped_tile(blockIdx.x, p.BH, p.num_pairs, p.group, pair, bh);
+  if (p.causal) pair = p.num_pairs - 1 - pair;
+  const int qs = pair * (C::TILES * C::BM);
+  const int nkb0 = tile_blocks(qs, p.n, p.m, p.causal);
+  const int nkb1 = tile_blocks(qs + C::BM, p.n, p.m, p.causal);
+  const int nkb = max(nkb0, nkb1);
 
   if (threadIdx.x == 0) {
     mbar_init(&bar[C::B_Q], 1);
@@ -111,11 +129,11 @@ __global__ void __launch_bounds__(256, 1)
       mbar_init(&bar[C::B_VF + s], 1);
       mbar_init(&bar[C::B_VE + s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bar[C::B_SF + b], 1);
-      mbar_init(&bar[C::B_PF + b], 128);
+    for (int t = 0; t < C::TILES; ++t) {
+      mbar_init(&bar[C::B_SF + t], 1);
+      mbar_init(&bar[C::B_PF + t], 128);
+      mbar_init(&bar[C::B_PVD + t], 1);
     }
-    mbar_init(&bar[C::B_OD], 1);
     mbar_init(&bar[C::B_DRAIN], 1);
     *abort_flag = 0u;
     fence_mbar_init();
@@ -135,10 +153,13 @@ __global__ void __launch_bounds__(256, 1)
       tma_prefetch_map(&tmQ);
       tma_prefetch_map(&tmK);
       tma_prefetch_map(&tmV);
-      mbar_arrive_expect_tx(&bar[C::B_Q], C::TILE);
+      mbar_arrive_expect_tx(&bar[C::B_Q], C::TILES * C::TILE);
 #pragma unroll
-      for (int c = 0; c < C::KCH; ++c)
-        tma_load_3d(smem + C::OFF_Q + c * C::CHUNK, &tmQ, &bar[C::B_Q], c * 64, qs, bh);
+      for (int t = 0; t < C::TILES; ++t)
+#pragma unroll
+        for (int c = 0; c < C::KCH; ++c)
+          tma_load_3d(smem + C::OFF_Q + t * C::TILE + c * C::CHUNK, &tmQ, &bar[C::B_Q], c * 64,
+                      qs + t * C::BM, bh);
       int nk = 0, nv = 0;  // loads issued
       for (int j = 0; j < nkb; ++j) {
         const int s = j % C::STAGES;
@@ -170,68 +191,70 @@ __global__ void __launch_bounds__(256, 1)
     // The whole warp runs the loop (operands stay warp-uniform); elect.sync picks
     // the issuing lane. Descriptors are built once per buffer and advanced by
     // compile-time byte offsets.
-    {
-      constexpr uint32_t kIdescS = idesc_bf16_f32(128, C::BN, false, false);
-      constexpr uint32_t kIdescO = idesc_bf16_f32(128, D, false, true);
-      const uint64_t dQ_k = sdesc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024);
-      bool ok = warp_wait(&bar[C::B_Q], 0, wc);
-      for (int j = 0; ok && j <= nkb; ++j) {
-        if (j < nkb) {
-          const int s = j % C::STAGES;
-          const int sb = j & 1;
-          if (!warp_wait(&bar[C::B_KF + s], (j / C::STAGES) & 1, wc)) break;
-          // S buffer sb was last read by the softmax of block j - 2.
-          if (j >= 2 && !warp_wait(&bar[C::B_PF + sb], ((j - 2) >> 1) & 1, wc)) break;
-          tc_fence_after();
-          const uint64_t dK_k = sdesc_sw128(smem_u32(smem + C::OFF_K + s * C::TILE), 16, 1024);
-          const uint32_t dS = tmem + (sb ? C::COL_S1 : C::COL_S0);
+    constexpr uint32_t kIdescS = idesc_bf16_f32(128, C::BN, false, false);
+    constexpr uint32_t kIdescO = idesc_bf16_f32(128, D, false, true);
+    bool ok = warp_wait(&bar[C::B_Q], 0, wc);
+    for (int j = 0; ok && j < nkb; ++j) {
+      const int s = j % C::STAGES;
+      const uint32_t ph = (j / C::STAGES) & 1;
+      if (!warp_wait(&bar[C::B_KF + s], ph, wc)) break;
+      const uint64_t dK_k = sdesc_sw128(smem_u32(smem + C::OFF_K + s * C::TILE), 16, 1024);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
-            umma_ss_w(dS, sdesc_add(dQ_k, off), sdesc_add(dK_k, off), kIdescS, kk > 0);
-          }
-          umma_commit_w(&bar[C::B_SF + sb]);
-          umma_commit_w(&bar[C::B_KE + s]);
-        }
-        if (j >= 1) {
-          const int jj = j - 1;
-          const int s = jj % C::STAGES;
-          const int pb = jj & 1;
-          if (!warp_wait(&bar[C::B_PF + pb], (jj >> 1) & 1, wc)) break;
-          if (!warp_wait(&bar[C::B_VF + s], (jj / C::STAGES) & 1, wc)) break;
-          tc_fence_after();
-          const uint64_t dV_mn =
-              sdesc_sw128(smem_u32(smem + C::OFF_V + s * C::TILE), C::CHUNK, 1024);
-          const uint32_t aP = tmem + (pb ? C::COL_P1 : C::COL_P0);
+      for (int t = 0; t < C::TILES; ++t) {
+        if (j >= (t == 0 ? nkb0 : nkb1)) continue;
+        // S_t's columns hold P_t of block j-1 until O_t += P_t V_{j-1} is done.
+        if (j >= 1 && !warp_wait(&bar[C::B_PVD + t], (j - 1) & 1, wc)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t dQ_k = sdesc_sw128(smem_u32(smem + C::OFF_Q + t * C::TILE), 16, 1024);
 #pragma unroll
-          for (int kk = 0; kk < C::BN / 16; ++kk)
-            umma_ts_w(tmem + C::COL_O, aP + kk * 8, sdesc_add(dV_mn, kk * 2048), kIdescO,
-                      (jj > 0 || kk > 0) ? 1u : 0u);
-          umma_commit_w(&bar[C::B_OD]);
-          umma_commit_w(&bar[C::B_VE + s]);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
+          umma_ss_w(tmem + C::COL_S + 128 * t, sdesc_add(dQ_k, off), sdesc_add(dK_k, off),
+                    kIdescS, kk > 0);
         }
+        umma_commit_w(&bar[C::B_SF + t]);
       }
-      umma_commit_w(&bar[C::B_DRAIN]);
-      drain_wait(&bar[C::B_DRAIN], 0);
+      if (!ok) break;
+      umma_commit_w(&bar[C::B_KE + s]);
+      if (!warp_wait(&bar[C::B_VF + s], ph, wc)) break;
+      const uint64_t dV_mn = sdesc_sw128(smem_u32(smem + C::OFF_V + s * C::TILE), C::CHUNK, 1024);
+#pragma unroll
+      for (int t = 0; t < C::TILES; ++t) {
+        if (j >= (t == 0 ? nkb0 : nkb1)) continue;
+        if (!warp_wait(&bar[C::B_PF + t], j & 1, wc)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t aP = tmem + C::COL_S + 128 * t;  // P_t: first 64 columns of S_t
+#pragma unroll
+        for (int kk = 0; kk < C::BN / 16; ++kk)
+          umma_ts_w(tmem + C::COL_O + D * t, aP + kk * 8, sdesc_add(dV_mn, kk * 2048), kIdescO,
+                    (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit_w(&bar[C::B_PVD + t]);
+      }
+      if (!ok) break;
+      umma_commit_w(&bar[C::B_VE + s]);
     }
+    umma_commit_w(&bar[C::B_DRAIN]);
+    drain_wait(&bar[C::B_DRAIN], 0);
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
-    const int row = (warp - 4) * 32 + lane;
+    const int t = (warp - 4) >> 2;                 // query tile of this warpgroup
+    const int row = ((warp - 4) & 3) * 32 + lane;  // row in the tile = TMEM lane
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    const int qg = qs + row;
+    const uint32_t scol = lane_base + C::COL_S + 128 * t;
+    const uint32_t ocol = lane_base + C::COL_O + D * t;
+    const int qg = qs + t * C::BM + row;
+    const int nkb_t = t == 0 ? nkb0 : nkb1;
     const float sl2 = p.scale_log2;
-    float m_run = -INFINITY;  // running max of S * scale * log2(e)
-    float l_run = 0.f;        // running sum of exp2(S * scale * log2(e) - m_run)
+    float m_ref = -INFINITY;  // reference maximum of S * scale * log2(e)
+    float l_run = 0.f;        // sum of exp2(S * scale * log2(e) - m_ref)
     bool ok = true;
-    for (int j = 0; j < nkb; ++j) {
-      const int sb = j & 1;
-      if (!warp_wait(&bar[C::B_SF + sb], (j >> 1) & 1, wc)) {
+    for (int j = 0; j < nkb_t; ++j) {
+      if (!warp_wait(&bar[C::B_SF + t], j & 1, wc)) {
         ok = false;
         break;
       }
       tc_fence_after();
       uint32_t sr[128];
-      const uint32_t scol = lane_base + (sb ? C::COL_S1 : C::COL_S0);
       tmem_ld32(scol + 0, sr);
       tmem_ld32(scol + 32, sr + 32);
       tmem_ld32(scol + 64, sr + 64);
@@ -251,65 +274,66 @@ __global__ void __launch_bounds__(256, 1)
         for (int c = 0; c < 128; ++c)
           if (c > lim) sr[c] = __float_as_uint(-INFINITY);
       }
-      float mx0 = -INFINITY, mx1 = -INFINITY;
+      float mx[8];
 #pragma unroll
-      for (int c = 0; c < 128; c += 2) {
-        mx0 = fmaxf(mx0, __uint_as_float(sr[c]));
-        mx1 = fmaxf(mx1, __uint_as_float(sr[c + 1]));
-      }
-      const float m_new = fmaxf(m_run, fmaxf(mx0, mx1) * sl2);
+      for (int k = 0; k < 8; ++k) mx[k] = __uint_as_float(sr[k]);
+#pragma unroll
+      for (int c = 8; c < 128; c += 8)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], __uint_as_float(sr[c + k]));
+      const float rmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
+      // Move the reference only when the row maximum passed it by the threshold.
+      const bool move = rmax > m_ref + kRescaleThreshold;
+      const float m_new = move ? rmax : m_ref;
+      const float corr = move ? ex2(m_ref - m_new) : 1.f;  // 0 on the first block
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;  // no (-inf) - (-inf)
-      const float corr = ex2(m_run - m_use);
-      float sum0 = 0.f, sum1 = 0.f;
+      float sum[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) sum[k] = 0.f;
       uint32_t pp[64];
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
         const float p0 = ex2(fmaf(__uint_as_float(sr[2 * c]), sl2, -m_use));
         const float p1 = ex2(fmaf(__uint_as_float(sr[2 * c + 1]), sl2, -m_use));
-        sum0 += p0;
-        sum1 += p1;
+        sum[(2 * c) & 7] += p0;
+        sum[(2 * c + 1) & 7] += p1;
         pp[c] = pack_bf16(p0, p1);
       }
-      l_run = l_run * corr + (sum0 + sum1);
-      m_run = m_new;
+      l_run = l_run * corr +
+              (((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7])));
+      m_ref = m_new;
 
-      // P buffer sb and the O accumulator are free once P_{j-1} V_{j-1} is done.
-      if (j >= 1) {
-        if (!warp_wait(&bar[C::B_OD], (j - 1) & 1, wc)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-      }
-      const uint32_t pcol = lane_base + (sb ? C::COL_P1 : C::COL_P0);
-      tmem_st32(pcol, pp);
-      tmem_st32(pcol + 32, pp + 32);
-      if (j >= 1 && __any_sync(0xffffffffu, corr != 1.f)) {
+      // S_t(j) completing implies O_t += P_t V_{j-1} completed (issued after it),
+      // so this row's S columns may take P and its O row may be rescaled.
+      tmem_st32(scol, pp);
+      tmem_st32(scol + 32, pp + 32);
+      if (j >= 1 && __any_sync(0xffffffffu, move)) {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
-          tmem_ld32(lane_base + C::COL_O + 32 * c, o);
+          tmem_ld32(ocol + 32 * c, o);
           tmem_ld_wait();
           reg_fence32(o);
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
-          tmem_st32(lane_base + C::COL_O + 32 * c, o);
+          tmem_st32(ocol + 32 * c, o);
         }
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bar[C::B_PF + sb]);
+      mbar_arrive(&bar[C::B_PF + t]);
     }
 
     // ------------------------------------------------------------ epilogue
-    if (ok && warp_wait(&bar[C::B_OD], (nkb - 1) & 1, wc)) {
+    if (ok && nkb_t > 0 && warp_wait(&bar[C::B_PVD + t], (nkb_t - 1) & 1, wc)) {
       tc_fence_after();
       const float inv_l = 1.f / l_run;
       __nv_bfloat16* orow = p.O + ((size_t)bh * p.n + qg) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
-        tmem_ld32(lane_base + C::COL_O + 32 * c, o);
+        tmem_ld32(ocol + 32 * c, o);
         tmem_ld_wait();
         reg_fence32(o);
         uint32_t w[16];
@@ -324,7 +348,7 @@ __global__ void __launch_bounds__(256, 1)
           dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
         }
       }
-      if (qg < p.n) p.L[(size_t)bh * p.n + qg] = (m_run + lg2(l_run)) * kLn2;
+      if (qg < p.n) p.L[(size_t)bh * p.n + qg] = (m_ref + lg2(l_run)) * kLn2;
     }
   }
 
@@ -351,13 +375,13 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
   p.m = a.m;
   p.BH = a.BH;
   p.causal = a.causal;
-  p.num_q_tiles = ceil_div(a.n, C::BM);
-  p.group = heads_per_group(a.BH, p.num_q_tiles);
+  p.num_pairs = ceil_div(a.n, C::TILES * C::BM);
+  p.group = heads_per_group(a.BH, p.num_pairs);
   p.scale_log2 = a.scale * 1.44269504088896340736f;
   cudaError_t e =
       cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  const unsigned grid = (unsigned)p.num_q_tiles * (unsigned)a.BH;
+  const unsigned grid = (unsigned)p.num_pairs * (unsigned)a.BH;
   fwd_kernel<D><<<grid, C::THREADS, C::SMEM, stream>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
