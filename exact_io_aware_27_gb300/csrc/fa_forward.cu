@@ -60,8 +60,8 @@ struct FwdCfg {
   static constexpr int B_VF = B_KE + STAGES;
   static constexpr int B_VE = B_VF + STAGES;
   static constexpr int B_SF = B_VE + STAGES;    // + tile: S_t ready
-  static constexpr int B_PF = B_SF + TILES;     // + tile: P_t written, O_t rescaled
-  static constexpr int B_PVD = B_PF + TILES;    // + tile: O_t += P_t V done
+  static constexpr int B_PF = B_SF + TILES;     // + 2 tile + half: half of P_t written
+  static constexpr int B_PVD = B_PF + 2 * TILES;  // + tile: O_t += P_t V done
   static constexpr int B_DRAIN = B_PVD + TILES;
   static constexpr int NBAR = B_DRAIN + 1;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;
@@ -131,7 +131,8 @@ __global__ void __launch_bounds__(384, 1)
     }
     for (int t = 0; t < C::TILES; ++t) {
       mbar_init(&bar[C::B_SF + t], 1);
-      mbar_init(&bar[C::B_PF + t], 128);
+      mbar_init(&bar[C::B_PF + 2 * t], 128);
+      mbar_init(&bar[C::B_PF + 2 * t + 1], 128);
       mbar_init(&bar[C::B_PVD + t], 1);
     }
     mbar_init(&bar[C::B_DRAIN], 1);
@@ -221,13 +222,18 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
       for (int t = 0; t < C::TILES; ++t) {
         if (j >= (t == 0 ? nkb0 : nkb1)) continue;
-        if (!warp_wait(&bar[C::B_PF + t], j & 1, wc)) { ok = false; break; }
-        tc_fence_after();
         const uint32_t aP = tmem + C::COL_S + 128 * t;  // P_t: first 64 columns of S_t
+        // Keys 0..63 as soon as their P is written, then keys 64..127.
 #pragma unroll
-        for (int kk = 0; kk < C::BN / 16; ++kk)
-          umma_ts_w(tmem + C::COL_O + D * t, aP + kk * 8, sdesc_add(dV_mn, kk * 2048), kIdescO,
-                    (j > 0 || kk > 0) ? 1u : 0u);
+        for (int h = 0; h < 2; ++h) {
+          if (!warp_wait(&bar[C::B_PF + 2 * t + h], j & 1, wc)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
+            umma_ts_w(tmem + C::COL_O + D * t, aP + kk * 8, sdesc_add(dV_mn, kk * 2048), kIdescO,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        if (!ok) break;
         umma_commit_w(&bar[C::B_PVD + t]);
       }
       if (!ok) break;
@@ -274,41 +280,56 @@ __global__ void __launch_bounds__(384, 1)
         for (int c = 0; c < 128; ++c)
           if (c > lim) sr[c] = __float_as_uint(-INFINITY);
       }
+      // Row maximum: eight chains of three-input maxima.
       float mx[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) mx[k] = __uint_as_float(sr[k]);
 #pragma unroll
-      for (int c = 8; c < 128; c += 8)
+      for (int c = 8; c < 128; c += 16)
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], __uint_as_float(sr[c + k]));
-      const float rmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
+        for (int k = 0; k < 8; ++k)
+          mx[k] = max3f(mx[k], __uint_as_float(sr[c + k]), __uint_as_float(sr[c + 8 + k]));
+      const float rmax = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]),
+                               fmaxf(mx[6], mx[7])) * sl2;
       // Move the reference only when the row maximum passed it by the threshold.
       const bool move = rmax > m_ref + kRescaleThreshold;
       const float m_new = move ? rmax : m_ref;
       const float corr = move ? ex2(m_ref - m_new) : 1.f;  // 0 on the first block
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;  // no (-inf) - (-inf)
-      float sum[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) sum[k] = 0.f;
-      uint32_t pp[64];
-#pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float p0 = ex2(fmaf(__uint_as_float(sr[2 * c]), sl2, -m_use));
-        const float p1 = ex2(fmaf(__uint_as_float(sr[2 * c + 1]), sl2, -m_use));
-        sum[(2 * c) & 7] += p0;
-        sum[(2 * c + 1) & 7] += p1;
-        pp[c] = pack_bf16(p0, p1);
-      }
-      l_run = l_run * corr +
-              (((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7])));
       m_ref = m_new;
-
-      // S_t(j) completing implies O_t += P_t V_{j-1} completed (issued after it),
-      // so this row's S columns may take P and its O row may be rescaled.
-      tmem_st32(scol, pp);
-      tmem_st32(scol + 32, pp + 32);
-      if (j >= 1 && __any_sync(0xffffffffu, move)) {
+      // S_t(j) completing implies O_t += P_t V_{j-1} completed (issued before
+      // it), so the O row may be rescaled before this block's products start.
+      // When no row of the warp moved its reference (the common case) each half
+      // of P is signalled as soon as it is written; otherwise both halves are
+      // signalled after the rescale.
+      const bool rescale = j >= 1 && __any_sync(0xffffffffu, move);
+      // P = exp2(S * scale * log2(e) - m) in two halves of 64 keys, written as
+      // bf16 pairs over this row's own S columns.
+      const uint64_t sl2x2 = f2pack(sl2, sl2);
+      const uint64_t negm2 = f2pack(-m_use, -m_use);
+      uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pp[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const int e = 64 * h + 2 * c;
+          const uint64_t x2 =
+              ffma2(f2pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sl2x2, negm2);
+          float x0, x1;
+          f2unpack(x2, x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          acc2[c & 3] = fadd2(acc2[c & 3], f2pack(p0, p1));
+          pp[c] = pack_bf16(p0, p1);
+        }
+        tmem_st32(scol + 32 * h, pp);
+        if (!rescale) {
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&bar[C::B_PF + 2 * t + h]);
+        }
+      }
+      if (rescale) {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
@@ -319,10 +340,17 @@ __global__ void __launch_bounds__(384, 1)
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
           tmem_st32(ocol + 32 * c, o);
         }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bar[C::B_PF + 2 * t]);
+        mbar_arrive(&bar[C::B_PF + 2 * t + 1]);
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&bar[C::B_PF + t]);
+      float s0, s1, s2, s3, s4, s5, s6, s7;
+      f2unpack(acc2[0], s0, s1);
+      f2unpack(acc2[1], s2, s3);
+      f2unpack(acc2[2], s4, s5);
+      f2unpack(acc2[3], s6, s7);
+      l_run = l_run * corr + (((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7)));
     }
 
     // ------------------------------------------------------------ epilogue
