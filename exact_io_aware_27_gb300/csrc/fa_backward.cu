@@ -68,11 +68,9 @@ struct BwdCfg {
   static constexpr int OFF_BAR = OFF_DQS + DQS_BYTES;
   // barrier slots
   static constexpr int B_KV = 0;
-  static constexpr int B_QF = 1;                // + stage
-  static constexpr int B_QE = B_QF + STAGES;    // + stage
-  static constexpr int B_OF = B_QE + STAGES;    // + stage
-  static constexpr int B_OE = B_OF + STAGES;    // + stage
-  static constexpr int B_SF = B_OE + STAGES;
+  static constexpr int B_QF = 1;                // + stage: Q_i, dO_i, L_i, D_i landed
+  static constexpr int B_QE = B_QF + STAGES;    // + stage: the stage may be refilled
+  static constexpr int B_SF = B_QE + STAGES;
   static constexpr int B_SFREE = B_SF + 1;
   static constexpr int B_PF = B_SF + 2;
   static constexpr int B_DVD = B_SF + 3;
@@ -142,8 +140,6 @@ __global__ void __launch_bounds__(512, 1)
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&bar[C::B_QF + s], 1);
       mbar_init(&bar[C::B_QE + s], 1);
-      mbar_init(&bar[C::B_OF + s], 1);
-      mbar_init(&bar[C::B_OE + s], 1);
     }
     mbar_init(&bar[C::B_SF], 1);
     mbar_init(&bar[C::B_SFREE], C::COMPUTE_THREADS);
@@ -179,33 +175,28 @@ __global__ void __launch_bounds__(512, 1)
         tma_load_3d(smem + C::OFF_K + c * C::KV_CHUNK, &tmK, &bar[C::B_KV], c * 64, ks, bh);
         tma_load_3d(smem + C::OFF_V + c * C::KV_CHUNK, &tmV, &bar[C::B_KV], c * 64, ks, bh);
       }
-      int nqi = 0, noi = 0;
+      int nqi = 0;
       for (int i = 0; i < nq; ++i) {
         const int s = i % C::STAGES;
         const uint32_t ph = (i / C::STAGES) & 1;
         const int q0 = (i_start + i) * C::BQ;
         if (i >= C::STAGES && !mbar_wait(&bar[C::B_QE + s], ph ^ 1, wc)) break;
-        mbar_arrive_expect_tx(&bar[C::B_QF + s], C::Q_TILE + 2 * C::BQ * 4);
+        mbar_arrive_expect_tx(&bar[C::B_QF + s], 2 * C::Q_TILE + 2 * C::BQ * 4);
 #pragma unroll
         for (int c = 0; c < C::KCH; ++c)
           tma_load_3d(smem + C::OFF_Q + s * C::Q_TILE + c * C::Q_CHUNK, &tmQ, &bar[C::B_QF + s],
                       c * 64, q0, bh);
         tma_load_2d(smem + C::OFF_LSE + s * C::BQ * 4, &tmL2, &bar[C::B_QF + s], q0, bh);
         tma_load_2d(smem + C::OFF_DD + s * C::BQ * 4, &tmD, &bar[C::B_QF + s], q0, bh);
-        nqi = i + 1;
-        if (i >= C::STAGES && !mbar_wait(&bar[C::B_OE + s], ph ^ 1, wc)) break;
-        mbar_arrive_expect_tx(&bar[C::B_OF + s], C::Q_TILE);
 #pragma unroll
         for (int c = 0; c < C::KCH; ++c)
           tma_load_3d(smem + C::OFF_DO + s * C::Q_TILE + c * C::Q_CHUNK, &tmdO,
-                      &bar[C::B_OF + s], c * 64, q0, bh);
-        noi = i + 1;
+                      &bar[C::B_QF + s], c * 64, q0, bh);
+        nqi = i + 1;
       }
       drain_wait(&bar[C::B_KV], 0);
       for (int i = max(0, nqi - C::STAGES); i < nqi; ++i)
         drain_wait(&bar[C::B_QF + i % C::STAGES], (i / C::STAGES) & 1);
-      for (int i = max(0, noi - C::STAGES); i < noi; ++i)
-        drain_wait(&bar[C::B_OF + i % C::STAGES], (i / C::STAGES) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -230,7 +221,6 @@ __global__ void __launch_bounds__(512, 1)
           const int s = i % C::STAGES;
           const uint32_t ph = (i / C::STAGES) & 1;
           if (!warp_wait(&bar[C::B_QF + s], ph, wc)) break;
-          if (!warp_wait(&bar[C::B_OF + s], ph, wc)) break;
           if (i >= 1 && !warp_wait(&bar[C::B_SFREE], (i - 1) & 1, wc)) break;
           tc_fence_after();
           const uint64_t dQ_k = sdesc_sw128(smem_u32(smem + C::OFF_Q + s * C::Q_TILE), 16, 1024);
@@ -262,7 +252,6 @@ __global__ void __launch_bounds__(512, 1)
             umma_ts_w(tmem + C::COL_DV, tmem + C::COL_P + kk * 8, sdesc_add(dO_mn, kk * 2048),
                       kIdescDV, (ii > 0 || kk > 0) ? 1u : 0u);
           umma_commit_w(&bar[C::B_DVD]);
-          umma_commit_w(&bar[C::B_OE + s]);
           // dK += dS^T Q_{i-1} and this block's share of dQ_{i-1}
           if (!warp_wait(&bar[C::B_DSF], ii & 1, wc)) break;
           if (ii >= 1 && !warp_wait(&bar[C::B_DQE], (ii - 1) & 1, wc)) break;

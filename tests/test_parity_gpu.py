@@ -102,6 +102,35 @@ def test_peaked_scores_and_custom_scale():
         parity.check_heads(Q, K, V, dO, causal, got, scale=0.05)
 
 
+def _growing_scores(B, H, n, m, d, growth, seed):
+    """Inputs whose scores rise along the key axis by about `growth` (natural
+    log units) from the first key to the last, on top of random parts. The
+    growth sits in Q's first feature (a constant) times a small ramp in K's, so
+    dQ = scale * dS K stays well conditioned (a large ramp in K would make dQ a
+    heavily cancelling sum that no bf16 dS can resolve to 1%)."""
+    Q, K, V, dO = wl.attention_inputs(B, H, n, m, d, seed=seed)
+    Q, K = Q.float(), K.float()
+    Q[..., 0] = growth
+    K[..., 0] = np.sqrt(d) * torch.arange(m, dtype=torch.float32) / m
+    return Q.to(torch.bfloat16), K.to(torch.bfloat16), V, dO
+
+
+@pytest.mark.parametrize("growth", [40.0, 4.0])
+def test_growing_row_maximum(growth):
+    # growth 40: the row maximum rises by ~12 (base 2) per 128-key block, past
+    # the forward's rescaling threshold of 8, so O and l are rescaled at every
+    # block; growth 4: it never passes the threshold after the first block and
+    # P reaches ~2^6 relative to the reference maximum.
+    Q, K, V, dO = _growing_scores(1, 2, 300, 700, 64, growth, seed=7950)
+    for causal in (False, True):
+        got = parity.run_gpu(Q, K, V, dO, causal)
+        parity.check_heads(Q, K, V, dO, causal, got)
+    Q, K, V, dO = _growing_scores(1, 1, 520, 520, 128, growth, seed=7960)
+    for causal in (False, True):
+        got = parity.run_gpu(Q, K, V, dO, causal)
+        parity.check_heads(Q, K, V, dO, causal, got)
+
+
 # ------------------------------------------------------------------ closed forms
 def test_zero_query_gives_uniform_attention():
     B, H, n, m, d = 1, 2, 190, 190, 64
