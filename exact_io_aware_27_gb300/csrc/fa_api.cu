@@ -162,7 +162,7 @@ int heads_per_group(int BH, int tiles_per_head) {
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int g = ceil_div(2 * sms, tiles_per_head > 0 ? tiles_per_head : 1);
+  const int g = ceil_div(8 * sms, tiles_per_head > 0 ? tiles_per_head : 1);
   return g < 1 ? 1 : (g > BH ? BH : g);
 }
 

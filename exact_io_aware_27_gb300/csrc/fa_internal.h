@@ -16,8 +16,10 @@ constexpr int kWorkspaceRowAlign = 128;
 inline int round_up(int x, int a) { return (x + a - 1) / a * a; }
 inline int ceil_div(int x, int a) { return (x + a - 1) / a; }
 
-// Heads per launch-order group (see grouped_tile): enough blocks for about two
-// waves over the SMs, so the blocks in flight touch few heads.
+// Heads per launch-order group (see grouped_tile): enough blocks for about eight
+// waves over the SMs. Smaller groups keep fewer heads' data in flight (less L2
+// traffic); larger ones let the heavy causal blocks of later heads start
+// earlier (a shorter tail). Eight waves measured best on GB300 for both kernels.
 int heads_per_group(int BH, int tiles_per_head);
 
 // cuTensorMapEncodeTiled, fetched from the driver at first use.
