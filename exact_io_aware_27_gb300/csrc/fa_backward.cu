@@ -53,9 +53,6 @@ struct BwdCfg {
   // dK reads dS^T from TMEM (the TS form) instead of shared memory; needs BQ/2
   // spare TMEM columns, which only the d = 128 layout has.
   static constexpr bool kDsInTmem = (D == 128);
-  // dQ partials staged in shared memory and added with one bulk reduction per
-  // block (true), or added straight from registers with fp32 reductions (false).
-  static constexpr bool kDqStaged = false;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + KV_TILE;
   static constexpr int OFF_Q = OFF_V + KV_TILE;
@@ -63,9 +60,7 @@ struct BwdCfg {
   static constexpr int OFF_DS = OFF_DO + STAGES * Q_TILE;
   static constexpr int OFF_LSE = OFF_DS + DS_TILE;          // [STAGES][BQ] fp32
   static constexpr int OFF_DD = OFF_LSE + STAGES * BQ * 4;  // [STAGES][BQ] fp32
-  static constexpr int OFF_DQS = OFF_DD + STAGES * BQ * 4;  // [BQ x D] fp32 dQ staging
-  static constexpr int DQS_BYTES = (D == 128 && kDqStaged) ? BQ * D * 4 : 0;
-  static constexpr int OFF_BAR = OFF_DQS + DQS_BYTES;
+  static constexpr int OFF_BAR = OFF_DD + STAGES * BQ * 4;
   // barrier slots
   static constexpr int B_KV = 0;
   static constexpr int B_QF = 1;                // + stage: Q_i, dO_i, L_i, D_i landed
@@ -478,8 +473,6 @@ __global__ void __launch_bounds__(512, 1)
     bool ok = true;
     for (int i = 0; i < nq; ++i) {
       const int q0 = (i_start + i) * C::BQ;
-      // Every thread of the group takes every iteration (also after an abort) so
-      // that the named barriers below always see all 128 threads.
       if (ok) ok = warp_wait(&bar[C::B_DSD], i & 1, wc);
       uint32_t v[64];
       if (ok) {
@@ -492,26 +485,7 @@ __global__ void __launch_bounds__(512, 1)
         tc_fence_before();
         mbar_arrive(&bar[C::B_DQE]);
       }
-      if (D == 128 && C::kDqStaged) {
-        // lane t = feature index, column = query. Stage the 64 x 128 fp32 block
-        // row-major in shared memory, then one thread adds it to the accumulator
-        // with a single 32 KB bulk reduction.
-        float* buf = reinterpret_cast<float*>(smem + C::OFF_DQS);
-        if (i >= 1) {
-          if (t == 0) bulk_wait_group_read<0>();  // the previous reduction has read buf
-          named_barrier(1, 128);
-        }
-        if (ok) {
-#pragma unroll
-          for (int q = 0; q < 64; ++q) buf[q * D + t] = __uint_as_float(v[q]);
-        }
-        fence_proxy_async_smem();
-        named_barrier(1, 128);
-        if (t == 0 && ok) {
-          bulk_reduce_add_f32(p.ws_dQ + ((size_t)bh * p.n_pad + q0) * D, buf, C::DQS_BYTES);
-          bulk_commit_group();
-        }
-      } else if (D == 128 && ok) {
+      if (D == 128 && ok) {
         // lane t = feature index, column = query: each warp adds 32 consecutive
         // floats of one accumulator row per instruction.
         float* base = p.ws_dQ + ((size_t)bh * p.n_pad + q0) * D + t;
@@ -527,7 +501,6 @@ __global__ void __launch_bounds__(512, 1)
                                           __uint_as_float(v[4 * c + 3])));
       }
     }
-    if (D == 128 && C::kDqStaged && t == 0) bulk_wait_group_all();  // reductions done before exit
   }
 
   tc_fence_before();

@@ -122,29 +122,6 @@ FA_DEV void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Bulk (non-tensor) reduction: global[dst .. dst+bytes) += shared[src ..] as
-// fp32, issued by one thread; both addresses 16-byte aligned, bytes a multiple
-// of 16. Tracked by the issuing thread's bulk async-group.
-FA_DEV void bulk_reduce_add_f32(float* gdst, const void* ssrc, uint32_t bytes) {
-  asm volatile(
-      "cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(gdst),
-      "r"(smem_u32(ssrc)), "r"(bytes)
-      : "memory");
-}
-FA_DEV void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Waits until at most N of this thread's bulk groups still read shared memory.
-template <int N>
-FA_DEV void bulk_wait_group_read() {
-  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-// Waits until all of this thread's bulk groups have completed (writes visible).
-FA_DEV void bulk_wait_group_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
-// Named barrier over `count` threads (a multiple of 32); id 0 is __syncthreads.
-FA_DEV void named_barrier(uint32_t id, uint32_t count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
 // ---------------------------------------------------------------- tcgen05
 FA_DEV void tmem_alloc(uint32_t* slot, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
