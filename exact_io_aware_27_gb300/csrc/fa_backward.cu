@@ -512,9 +512,11 @@ __global__ void __launch_bounds__(512, 1)
 }
 
 // ------------------------------------------------------------------ preprocess
-// One warp per workspace row (head bh, query q < n_pad): D = sum_c dO*O,
-// L2 = L * log2(e), and the dQ accumulator row cleared. Rows q >= n get
-// D = 0 and L2 = +inf so that recomputed probabilities there are exactly 0.
+// Each warp step covers RPW consecutive workspace rows (head bh, query q <
+// n_pad), LPR lanes per row, one 16-byte load of O and of dO per lane:
+// D = sum_c dO*O, L2 = L * log2(e), and the rows' dQ accumulator cleared. Rows
+// q >= n get D = 0 and L2 = +inf so that recomputed probabilities there are
+// exactly 0.
 template <int D>
 __global__ void __launch_bounds__(256) preprocess_kernel(const __nv_bfloat16* __restrict__ O,
                                                          const __nv_bfloat16* __restrict__ dO,
@@ -523,60 +525,60 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const __nv_bfloat16* __
                                                          float* __restrict__ ws_L2,
                                                          float* __restrict__ ws_dQ, int n,
                                                          int n_pad, long long rows) {
+  constexpr int LPR = D / 8;       // lanes per row (8 bf16 per lane)
+  constexpr int RPW = 32 / LPR;    // rows per warp step
   const int lane = threadIdx.x & 31;
+  const int sub = lane % LPR;
   const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
-  for (long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;
-       r += warps) {
+  for (long long base = ((long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * RPW;
+       base < rows; base += warps * RPW) {
+    const long long r = base + lane / LPR;  // rows is a multiple of RPW (n_pad % 128 == 0)
     const long long bh = r / n_pad;
     const int q = (int)(r - bh * n_pad);
     float acc = 0.f;
     if (q < n) {
       const size_t off = ((size_t)bh * n + q) * D;
-      if (D == 128) {
-        const uint2 a = reinterpret_cast<const uint2*>(O + off)[lane];
-        const uint2 b = reinterpret_cast<const uint2*>(dO + off)[lane];
-        acc = bf16_lo(a.x) * bf16_lo(b.x) + bf16_hi(a.x) * bf16_hi(b.x) +
-              bf16_lo(a.y) * bf16_lo(b.y) + bf16_hi(a.y) * bf16_hi(b.y);
-      } else {
-        const uint32_t a = reinterpret_cast<const uint32_t*>(O + off)[lane];
-        const uint32_t b = reinterpret_cast<const uint32_t*>(dO + off)[lane];
-        acc = bf16_lo(a) * bf16_lo(b) + bf16_hi(a) * bf16_hi(b);
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      const uint4 a = reinterpret_cast<const uint4*>(O + off)[sub];
+      const uint4 b = reinterpret_cast<const uint4*>(dO + off)[sub];
+      acc = bf16_lo(a.x) * bf16_lo(b.x) + bf16_hi(a.x) * bf16_hi(b.x) +
+            bf16_lo(a.y) * bf16_lo(b.y) + bf16_hi(a.y) * bf16_hi(b.y) +
+            bf16_lo(a.z) * bf16_lo(b.z) + bf16_hi(a.z) * bf16_hi(b.z) +
+            bf16_lo(a.w) * bf16_lo(b.w) + bf16_hi(a.w) * bf16_hi(b.w);
     }
-    if (lane == 0) {
+#pragma unroll
+    for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (sub == 0) {
       ws_D[r] = acc;
       ws_L2[r] = (q < n) ? L[(size_t)bh * n + q] * kLog2e : INFINITY;
     }
-    float* drow = ws_dQ + (size_t)r * D;
-    if (D == 128) {
-      reinterpret_cast<float4*>(drow)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
-    } else {
-      reinterpret_cast<float2*>(drow)[lane] = make_float2(0.f, 0.f);
-    }
+    // the RPW rows' accumulator (RPW * D floats = 1 KB): two float4 per lane
+    float4* drow = reinterpret_cast<float4*>(ws_dQ + (size_t)base * D);
+    drow[2 * lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+    drow[2 * lane + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 }
 
 // ------------------------------------------------------------------ dQ convert
-// dQ[bh, q, :] = bf16(accumulator[bh, q, :] * scale) for q < n; 8 values per thread.
+// dQ[bh, q, :] = bf16(accumulator[bh, q, :] * scale) for q < n; 16 values per thread.
 __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ ws_dQ,
                                                          __nv_bfloat16* __restrict__ dQ, int n,
                                                          int n_pad, int d, float scale,
                                                          long long groups) {
   const long long stride = (long long)gridDim.x * blockDim.x;
-  const int gpr = d / 8;  // groups of 8 per row
+  const int gpr = d / 16;  // groups of 16 per row
   for (long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x; g < groups; g += stride) {
     const long long row = g / gpr;  // over BH * n
-    const int c8 = (int)(g - row * gpr);
+    const int c16 = (int)(g - row * gpr);
     const long long bh = row / n;
     const int q = (int)(row - bh * n);
     const float4* src =
-        reinterpret_cast<const float4*>(ws_dQ + ((size_t)bh * n_pad + q) * d) + 2 * c8;
-    const float4 a = src[0], b = src[1];
-    reinterpret_cast<uint4*>(dQ + (size_t)row * d)[c8] =
-        make_uint4(pack_bf16(a.x * scale, a.y * scale), pack_bf16(a.z * scale, a.w * scale),
-                   pack_bf16(b.x * scale, b.y * scale), pack_bf16(b.z * scale, b.w * scale));
+        reinterpret_cast<const float4*>(ws_dQ + ((size_t)bh * n_pad + q) * d) + 4 * c16;
+    const float4 a = src[0], b = src[1], c = src[2], e = src[3];
+    uint4* dst = reinterpret_cast<uint4*>(dQ + (size_t)row * d) + 2 * c16;
+    dst[0] = make_uint4(pack_bf16(a.x * scale, a.y * scale), pack_bf16(a.z * scale, a.w * scale),
+                        pack_bf16(b.x * scale, b.y * scale), pack_bf16(b.z * scale, b.w * scale));
+    dst[1] = make_uint4(pack_bf16(c.x * scale, c.y * scale), pack_bf16(c.z * scale, c.w * scale),
+                        pack_bf16(e.x * scale, e.y * scale), pack_bf16(e.z * scale, e.w * scale));
   }
 }
 
@@ -623,7 +625,7 @@ int grid_for(long long work_items, int per_block) {
 
 cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t s) {
   const long long rows = (long long)a.BH * a.n_pad;
-  const int grid = grid_for(rows, 8);
+  const int grid = grid_for(rows / (a.d == 128 ? 2 : 4), 8);  // warp steps, 8 warps a block
   if (a.d == 128)
     preprocess_kernel<128><<<grid, 256, 0, s>>>(
         static_cast<const __nv_bfloat16*>(a.O), static_cast<const __nv_bfloat16*>(a.dO), a.L,
@@ -640,7 +642,7 @@ cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t s) {
-  const long long groups = (long long)a.BH * a.n * (a.d / 8);
+  const long long groups = (long long)a.BH * a.n * (a.d / 16);
   dq_convert_kernel<<<grid_for(groups, 256), 256, 0, s>>>(
       a.ws_dQ, static_cast<__nv_bfloat16*>(a.dQ), a.n, a.n_pad, a.d, a.scale, groups);
   return cudaGetLastError();
