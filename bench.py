@@ -258,7 +258,7 @@ def run_ours(args):
         fa.fa_backward_dkdv(q, k, v, do, ws, causal=w.causal, dK=dK, dV=dV)
         if ev is not None:
             ev[3].record(stream)
-        fa.fa_backward_dq(B, H, n, m, d, ws, dQ=dQ)
+        fa.fa_backward_dq(q, k, v, do, ws, causal=w.causal, dQ=dQ)
         if ev is not None:
             ev[4].record(stream)
 
@@ -309,8 +309,11 @@ def run_ours(args):
     peak = peaks["bf16_tflops_sustained"]
 
     # Dominant kernel and its roofline.
-    names = ["forward", "bwd_preprocess", "bwd_dkdv", "bwd_dq_convert"]
-    flops = [w.flops_fwd(), 0.0, w.flops_bwd(), 0.0]
+    # Tensor work each kernel executes, in units of the forward's 4*n*m*d:
+    # dkdv forms S^T, dP^T, dV, dK (2.0); dq forms S, dP, dQ (1.5, of which S and
+    # dP are the recompute that replaces reductions into dQ in memory).
+    names = ["forward", "bwd_preprocess", "bwd_dkdv", "bwd_dq"]
+    flops = [w.flops_fwd(), 0.0, 2.0 * w.flops_fwd(), 1.5 * w.flops_fwd()]
     top = max(range(4), key=lambda j: stage[j])
     if flops[top] > 0:
         ach = flops[top] / (stage[top] * 1e-3) / 1e12
@@ -330,10 +333,8 @@ def run_ours(args):
             entry["tflops"] = flops[j] / (stage[j] * 1e-3) / 1e12
         kernels[nm] = entry
     bpe = 2
-    pre_bytes = 2 * B * H * n * d * bpe + B * H * n * 4 * 3 + B * H * n * d * 4
+    pre_bytes = 2 * B * H * n * d * bpe + B * H * n * 4 * 3  # read O, dO, L; write -D, -L2
     kernels["bwd_preprocess"]["gbs"] = pre_bytes / (stage[1] * 1e-3) / 1e9
-    cvt_bytes = B * H * n * d * (4 + bpe)
-    kernels["bwd_dq_convert"]["gbs"] = cvt_bytes / (stage[3] * 1e-3) / 1e9
 
     e2e = None
     if not args.no_e2e:

@@ -41,7 +41,7 @@ SIGNATURES = {
                          _S, _P]),
     "fa_backward_preprocess": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _S, _P]),
     "fa_backward_dkdv": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _S, _P]),
-    "fa_backward_dq": (_I, [_I, _I, _I, _I, _I, _F, _P, _P, _S, _P]),
+    "fa_backward_dq": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _S, _P]),
     "fa_backward_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P,
                                  _P, _P]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
@@ -163,7 +163,7 @@ def fa_backward(Q, K, V, O, L, dO, causal: bool = False, scale: float | None = N
     return dQ, dK, dV
 
 
-NOALLOC_WORKSPACE_BYTES = 32 * 1024 * 1024
+NOALLOC_WORKSPACE_BYTES = 1024 * 1024
 
 
 def fa_backward_noalloc(Q, K, V, O, L, dO, causal: bool = False, scale: float | None = None,
@@ -209,11 +209,13 @@ def fa_backward_dkdv(Q, K, V, dO, workspace, causal=False, scale=None, dK=None, 
     return dK, dV
 
 
-def fa_backward_dq(B, H, n, m, d, workspace, scale=None, dQ=None, stream=None):
-    if dQ is None:
-        dQ = torch.empty((B, H, n, d), dtype=torch.bfloat16, device=workspace.device)
-    rc = lib().fa_backward_dq(B, H, n, m, d, _scale(scale, d), dQ.data_ptr(),
-                              workspace.data_ptr(), workspace.numel(), _stream(dQ, stream))
+def fa_backward_dq(Q, K, V, dO, workspace, causal=False, scale=None, dQ=None, stream=None):
+    B, H, n, d = Q.shape
+    m = K.shape[2]
+    dQ = torch.empty_like(Q) if dQ is None else dQ
+    rc = lib().fa_backward_dq(Q.data_ptr(), K.data_ptr(), V.data_ptr(), dO.data_ptr(), B, H, n,
+                              m, d, int(bool(causal)), _scale(scale, d), dQ.data_ptr(),
+                              workspace.data_ptr(), workspace.numel(), _stream(Q, stream))
     _check("fa_backward_dq", rc)
     return dQ
 

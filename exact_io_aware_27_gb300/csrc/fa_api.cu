@@ -79,22 +79,20 @@ int check_scale(float scale) {
 }
 
 struct Workspace {
-  float* D;
-  float* L2;
-  float* dQ;
+  float* nD;
+  float* nL2;
   size_t bytes;
   int n_pad;
 };
 
-Workspace workspace_layout(void* base, int B, int H, int n, int d) {
+Workspace workspace_layout(void* base, int B, int H, int n) {
   Workspace w;
   w.n_pad = round_up(n, kWorkspaceRowAlign);
   const size_t rows = (size_t)B * H * w.n_pad;
   float* f = static_cast<float*>(base);
-  w.D = f;
-  w.L2 = f + rows;
-  w.dQ = f + 2 * rows;
-  w.bytes = rows * (2 + (size_t)d) * sizeof(float);
+  w.nD = f;
+  w.nL2 = f + rows;
+  w.bytes = rows * 2 * sizeof(float);
   return w;
 }
 
@@ -115,7 +113,7 @@ int prepare_backward(const void* Q, const void* K, const void* V, const void* O,
   for (const void* ptr : bf16s)
     if (ptr && !aligned(ptr, 16)) return FA_ERR_MISALIGNED;
   if (L && !aligned(L, 4)) return FA_ERR_MISALIGNED;
-  const Workspace w = workspace_layout(workspace, B, H, n, d);
+  const Workspace w = workspace_layout(workspace, B, H, n);
   if (workspace_bytes < w.bytes) return FA_ERR_WORKSPACE_TOO_SMALL;
   const size_t qn = (size_t)B * H * n * d * 2, km = (size_t)B * H * m * d * 2;
   const Range ins[] = {Q ? range_of(Q, qn) : Range{0, 0},  K ? range_of(K, km) : Range{0, 0},
@@ -143,9 +141,8 @@ int prepare_backward(const void* Q, const void* K, const void* V, const void* O,
   a->dQ = dQ;
   a->dK = dK;
   a->dV = dV;
-  a->ws_D = w.D;
-  a->ws_L2 = w.L2;
-  a->ws_dQ = w.dQ;
+  a->ws_nD = w.nD;
+  a->ws_nL2 = w.nL2;
   a->BH = B * H;
   a->n = n;
   a->m = m;
@@ -248,7 +245,7 @@ int fa_forward(const void* Q, const void* K, const void* V, int B, int H, int n,
 
 size_t fa_backward_workspace_size(int B, int H, int n, int m, int d) {
   if (check_sizes(B, H, n, m, d) != FA_OK) return 0;
-  return workspace_layout(nullptr, B, H, n, d).bytes;
+  return workspace_layout(nullptr, B, H, n).bytes;
 }
 
 int fa_backward_preprocess(const void* O, const void* dO, const float* L, int B, int H, int n,
@@ -273,13 +270,13 @@ int fa_backward_dkdv(const void* Q, const void* K, const void* V, const void* dO
   return from_cuda(launch_bwd_dkdv(a, static_cast<cudaStream_t>(stream)));
 }
 
-int fa_backward_dq(int B, int H, int n, int m, int d, float scale, void* dQ,
-                   const void* workspace, size_t workspace_bytes, void* stream) {
-  if (!dQ) return FA_ERR_INVALID_ARG;
+int fa_backward_dq(const void* Q, const void* K, const void* V, const void* dO, int B, int H,
+                   int n, int m, int d, int causal, float scale, void* dQ, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+  if (!Q || !K || !V || !dO || !dQ) return FA_ERR_INVALID_ARG;
   BwdArgs a;
-  const int rc = prepare_backward(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, B, H, n,
-                                  m, d, 0, scale, dQ, nullptr, nullptr,
-                                  const_cast<void*>(workspace), workspace_bytes, false, false,
+  const int rc = prepare_backward(Q, K, V, nullptr, nullptr, dO, B, H, n, m, d, causal, scale,
+                                  dQ, nullptr, nullptr, workspace, workspace_bytes, false, false,
                                   &a);
   if (rc != FA_OK) return rc;
   return from_cuda(launch_bwd_dq(a, static_cast<cudaStream_t>(stream)));

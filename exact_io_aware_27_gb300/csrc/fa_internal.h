@@ -8,9 +8,9 @@
 
 namespace fa {
 
-// Rows of the fp32 workspace arrays (D, scaled L, dQ accumulator) per head:
-// n rounded up to a multiple of this, so that every tile the kernels touch is
-// in bounds and every row stride is a multiple of 16 bytes.
+// Rows of the fp32 workspace arrays (-D and -L * log2(e)) per head: n rounded
+// up to a multiple of this, so that every tile the kernels touch is in bounds
+// and every row stride is a multiple of 16 bytes.
 constexpr int kWorkspaceRowAlign = 128;
 
 inline int round_up(int x, int a) { return (x + a - 1) / a * a; }
@@ -46,9 +46,8 @@ struct BwdArgs {
   const void *Q, *K, *V, *O, *dO;
   const float* L;
   void *dQ, *dK, *dV;
-  float* ws_D;    // [BH, n_pad] fp32
-  float* ws_L2;   // [BH, n_pad] fp32, L * log2(e); +inf in the padding
-  float* ws_dQ;   // [BH, n_pad, d] fp32
+  float* ws_nD;   // [BH, n_pad] fp32, -D; 0 in the padding
+  float* ws_nL2;  // [BH, n_pad] fp32, -L * log2(e); -inf in the padding
   int BH, n, m, d, n_pad, causal;
   float scale;
 };

@@ -311,6 +311,11 @@ FA_DEV uint64_t fadd2(uint64_t a, uint64_t b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
+FA_DEV uint64_t fmul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 
 // Two floats -> packed bf16 pair (round to nearest even); `lo` in bits 0..15.
 FA_DEV uint32_t pack_bf16(float lo, float hi) {

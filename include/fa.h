@@ -74,9 +74,10 @@ FA_API int fa_forward(const void* Q, const void* K, const void* V, int B, int H,
                int d, int causal, float scale, void* O, float* L, void* stream);
 
 /*
- * Bytes of device workspace fa_backward needs: D and a pre-scaled copy of L
- * (fp32 [B, H, n_pad] each) and an fp32 dQ accumulator [B, H, n_pad, d], with
- * n_pad = n rounded up to a multiple of 128. Returns 0 for invalid sizes.
+ * Bytes of device workspace fa_backward needs: -D and -L * log2(e) (fp32
+ * [B, H, n_pad] each, n_pad = n rounded up to a multiple of 128), 8 bytes per
+ * padded query row. m and d are checked but do not change the size. Returns 0
+ * for invalid sizes.
  */
 FA_API size_t fa_backward_workspace_size(int B, int H, int n, int m, int d);
 
@@ -95,23 +96,28 @@ FA_API int fa_backward(const void* Q, const void* K, const void* V, const void* 
 
 /*
  * The three stages of fa_backward, callable one by one (same arguments and
- * rules as fa_backward; each must see the workspace the previous one wrote).
+ * rules as fa_backward). fa_backward_dkdv and fa_backward_dq read the workspace
+ * fa_backward_preprocess wrote and do not modify it, so they may run in either
+ * order once it is complete.
  *
  * fa_backward_preprocess: D = rowsum(dO o O) per query row (the first line of
- *   flash_attention_backward), L * log2(e) for the recompute, and a zeroed
- *   dQ accumulator, all into the workspace. Memory bound.
+ *   flash_attention_backward) and L * log2(e) for the recompute, stored
+ *   negated, into the workspace. Memory bound.
  * fa_backward_dkdv: per key block, loop over query blocks; rebuild P from L,
- *   accumulate dV = P^T dO and dK = dS^T Q * scale on chip and write them
- *   once; add each block's dS K into the fp32 dQ accumulator.
- * fa_backward_dq: dQ = bf16(accumulator * scale).
+ *   accumulate dV = P^T dO and dK = dS^T Q * scale on chip and write them once.
+ * fa_backward_dq: per query block, loop over key blocks; rebuild P and dP,
+ *   accumulate dQ = dS K * scale on chip and write it once (the pages add dS K
+ *   into dQ from inside the key loop; this computes the same sum as its own
+ *   pass, with no read-modify-write of dQ in memory).
  */
 FA_API int fa_backward_preprocess(const void* O, const void* dO, const float* L, int B, int H, int n,
                            int d, void* workspace, size_t workspace_bytes, void* stream);
 FA_API int fa_backward_dkdv(const void* Q, const void* K, const void* V, const void* dO, int B, int H,
                      int n, int m, int d, int causal, float scale, void* dK, void* dV,
                      void* workspace, size_t workspace_bytes, void* stream);
-FA_API int fa_backward_dq(int B, int H, int n, int m, int d, float scale, void* dQ,
-                   const void* workspace, size_t workspace_bytes, void* stream);
+FA_API int fa_backward_dq(const void* Q, const void* K, const void* V, const void* dO, int B, int H,
+                   int n, int m, int d, int causal, float scale, void* dQ, void* workspace,
+                   size_t workspace_bytes, void* stream);
 
 /*
  * Backward pass without a caller-supplied workspace (the pages have no
@@ -126,12 +132,12 @@ FA_API int fa_backward_dq(int B, int H, int n, int m, int d, float scale, void* 
  * whole device. Such callers still pass their own inputs and outputs.
  *
  * Instead of a caller buffer it uses one statically sized array in device
- * global memory inside this library: FA_NOALLOC_WORKSPACE_BYTES (32 MiB), held
+ * global memory inside this library: FA_NOALLOC_WORKSPACE_BYTES (1 MiB), held
  * on every GPU that loads the library until the process exits. Problems whose
- * workspace (fa_backward_workspace_size) exceeds it are rejected with
- * FA_ERR_WORKSPACE_TOO_SMALL before anything is queued; for example
- * B*H = 64 heads of n = 1024, d = 64 fit, but B*H = 64 heads of n = 4096,
- * d = 128 do not. This call allocates nothing: no cudaMalloc, no cudaFree, no
+ * workspace (fa_backward_workspace_size, 8 bytes per padded query row) exceeds
+ * it are rejected with FA_ERR_WORKSPACE_TOO_SMALL before anything is queued;
+ * for example B*H = 64 heads of n = 2048 fit, but B*H = 64 heads of n = 4096
+ * do not. This call allocates nothing: no cudaMalloc, no cudaFree, no
  * allocating library routine.
  *
  * The first call on a device looks up the array's device address on that
@@ -142,7 +148,7 @@ FA_API int fa_backward_dq(int B, int H, int n, int m, int d, float scale, void* 
  * example on two streams without ordering between them) race on the array
  * and give undefined results: order them on one stream or with events.
  */
-#define FA_NOALLOC_WORKSPACE_BYTES (32u * 1024u * 1024u)
+#define FA_NOALLOC_WORKSPACE_BYTES (1024u * 1024u)
 FA_API int fa_backward_noalloc(const void* Q, const void* K, const void* V, const void* O,
                                const float* L, const void* dO, int B, int H, int n, int m, int d,
                                int causal, float scale, void* dQ, void* dK, void* dV,

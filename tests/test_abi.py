@@ -45,10 +45,10 @@ def test_status_strings(lib):
 
 
 def test_workspace_size(lib):
-    # D and scaled L (n_pad floats each) plus the dQ accumulator (n_pad * d floats)
-    assert fa.fa_backward_workspace_size(2, 3, 100, 50, 64) == 2 * 3 * 128 * (2 + 64) * 4
-    assert fa.fa_backward_workspace_size(1, 1, 128, 128, 128) == 128 * 130 * 4
-    assert fa.fa_backward_workspace_size(1, 1, 129, 7, 128) == 256 * 130 * 4
+    # -D and -L * log2(e): n_pad floats each per head, n_pad = n rounded up to 128
+    assert fa.fa_backward_workspace_size(2, 3, 100, 50, 64) == 2 * 3 * 128 * 2 * 4
+    assert fa.fa_backward_workspace_size(1, 1, 128, 128, 128) == 128 * 2 * 4
+    assert fa.fa_backward_workspace_size(1, 1, 129, 7, 128) == 256 * 2 * 4
     assert fa.fa_backward_workspace_size(1, 1, 0, 7, 128) == 0
     assert fa.fa_backward_workspace_size(1, 1, 8, 7, 96) == 0
 

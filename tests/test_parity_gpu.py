@@ -220,8 +220,7 @@ def test_autograd_wrapper_matches_direct_calls():
     dQ, dK, dV = fa.fa_backward(Q, K, V, O, L, dO, True)
     torch.cuda.synchronize()
     assert torch.equal(out.detach(), O)
-    assert torch.equal(k.grad, dK) and torch.equal(v.grad, dV)
-    assert float((q.grad.float() - dQ.float()).abs().max()) <= 1e-2
+    assert torch.equal(k.grad, dK) and torch.equal(v.grad, dV) and torch.equal(q.grad, dQ)
 
 
 def test_stage_entry_points_match_fa_backward():
@@ -231,11 +230,10 @@ def test_stage_entry_points_match_fa_backward():
     dQ, dK, dV = fa.fa_backward(Q, K, V, O, L, dO, True)
     ws = fa.alloc_workspace(B, H, n, m, d, Q.device)
     fa.fa_backward_preprocess(O, dO, L, ws)
+    dQ2 = fa.fa_backward_dq(Q, K, V, dO, ws, causal=True)  # either order after preprocess
     dK2, dV2 = fa.fa_backward_dkdv(Q, K, V, dO, ws, causal=True)
-    dQ2 = fa.fa_backward_dq(B, H, n, m, d, ws)
     torch.cuda.synchronize()
-    assert torch.equal(dK, dK2) and torch.equal(dV, dV2)
-    assert float((dQ.float() - dQ2.float()).abs().max()) <= 1e-2
+    assert torch.equal(dK, dK2) and torch.equal(dV, dV2) and torch.equal(dQ, dQ2)
 
 
 def test_repeatable_and_no_timeout():
@@ -246,6 +244,6 @@ def test_repeatable_and_no_timeout():
     r2 = fa.fa_backward(Q, K, V, O1, L1, dO, True)
     torch.cuda.synchronize()
     assert torch.equal(O1, O2) and torch.equal(L1, L2)
-    assert torch.equal(r1[1], r2[1]) and torch.equal(r1[2], r2[2])
-    assert float((r1[0].float() - r2[0].float()).abs().max()) <= 1e-2
+    for a, b in zip(r1, r2):  # no atomics anywhere: identical bits
+        assert torch.equal(a, b)
     assert fa.fa_get_device_status() == 0

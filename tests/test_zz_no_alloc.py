@@ -53,8 +53,9 @@ def test_noalloc_matches_fa_backward_twice(B, H, n, m, d, causal, seed):
         for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
             assert torch.isfinite(g.float()).all(), f"call {call}: {name} not fully written"
             assert _rel(g, r) <= TOL, f"call {call}: {name} differs: {_rel(g, r):.3e}"
-        # dK and dV do not depend on accumulation order: identical bits
-        assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2])
+        # no reduction depends on scheduling order: identical bits
+        for g, r in zip(got, ref):
+            assert torch.equal(g, r)
     assert fa.fa_get_device_status() == 0
 
 
