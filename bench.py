@@ -255,12 +255,9 @@ def run_ours(args):
         fa.fa_backward_preprocess(O, do, L, ws)
         if ev is not None:
             ev[2].record(stream)
-        fa.fa_backward_dkdv(q, k, v, do, ws, causal=w.causal, dK=dK, dV=dV)
+        fa.fa_backward_grads(q, k, v, do, ws, causal=w.causal, dQ=dQ, dK=dK, dV=dV)
         if ev is not None:
             ev[3].record(stream)
-        fa.fa_backward_dq(q, k, v, do, ws, causal=w.causal, dQ=dQ)
-        if ev is not None:
-            ev[4].record(stream)
 
     def barrier():
         if world > 1:
@@ -273,7 +270,7 @@ def run_ours(args):
     if fa.fa_get_device_status() != 0:
         raise RuntimeError("device barrier timeout during warm-up")
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     clocks = ClockSampler(dev)
     clocks.start()
     time.sleep(0.2)
@@ -289,9 +286,9 @@ def run_ours(args):
     barrier()
     clk = clocks.stop()
     elapsed_ms = t_start.elapsed_time(t_end)
-    stage = [0.0] * 4
+    stage = [0.0] * 3
     for e in evs:
-        for j in range(4):
+        for j in range(3):
             stage[j] += e[j].elapsed_time(e[j + 1])
     stage = [s / args.steps for s in stage]
     elapsed_ms = max_over_ranks(elapsed_ms, dev)
@@ -309,12 +306,13 @@ def run_ours(args):
     peak = peaks["bf16_tflops_sustained"]
 
     # Dominant kernel and its roofline.
-    # Tensor work each kernel executes, in units of the forward's 4*n*m*d:
-    # dkdv forms S^T, dP^T, dV, dK (2.0); dq forms S, dP, dQ (1.5, of which S and
-    # dP are the recompute that replaces reductions into dQ in memory).
-    names = ["forward", "bwd_preprocess", "bwd_dkdv", "bwd_dq"]
-    flops = [w.flops_fwd(), 0.0, 2.0 * w.flops_fwd(), 1.5 * w.flops_fwd()]
-    top = max(range(4), key=lambda j: stage[j])
+    # Algorithmic FLOPs per kernel (the backward's 2.5x the forward all fall in
+    # the gradient kernel). That kernel executes 3.5x: S^T, dP^T, dV, dK for
+    # dK/dV (2.0) and S, dP, dQ for dQ (1.5, of which S and dP are the
+    # recompute that replaces reductions into dQ in memory); reported apart.
+    names = ["forward", "bwd_preprocess", "bwd_grads"]
+    flops = [w.flops_fwd(), 0.0, w.flops_bwd()]
+    top = max(range(3), key=lambda j: stage[j])
     if flops[top] > 0:
         ach = flops[top] / (stage[top] * 1e-3) / 1e12
         traffic = _traffic(names[top]) if w.name == WORKLOAD.name else None
@@ -332,6 +330,7 @@ def run_ours(args):
         if flops[j] > 0:
             entry["tflops"] = flops[j] / (stage[j] * 1e-3) / 1e12
         kernels[nm] = entry
+    kernels["bwd_grads"]["tflops_executed"] = 3.5 * w.flops_fwd() / (stage[2] * 1e-3) / 1e12
     bpe = 2
     pre_bytes = 2 * B * H * n * d * bpe + B * H * n * 4 * 3  # read O, dO, L; write -D, -L2
     kernels["bwd_preprocess"]["gbs"] = pre_bytes / (stage[1] * 1e-3) / 1e9
@@ -395,7 +394,7 @@ def run_ours(args):
             "roofline": roof,
             "kernels": kernels,
             "e2e": e2e,
-            "gpu_launches": 4 * args.steps,
+            "gpu_launches": 3 * args.steps,
             "clocks": clk,
             "cpu_baseline": cpu,
         }

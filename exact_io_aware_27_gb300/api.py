@@ -42,6 +42,8 @@ SIGNATURES = {
     "fa_backward_preprocess": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _S, _P]),
     "fa_backward_dkdv": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _S, _P]),
     "fa_backward_dq": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _S, _P]),
+    "fa_backward_grads": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _S,
+                               _P]),
     "fa_backward_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P,
                                  _P, _P]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
@@ -218,6 +220,22 @@ def fa_backward_dq(Q, K, V, dO, workspace, causal=False, scale=None, dQ=None, st
                               workspace.data_ptr(), workspace.numel(), _stream(Q, stream))
     _check("fa_backward_dq", rc)
     return dQ
+
+
+def fa_backward_grads(Q, K, V, dO, workspace, causal=False, scale=None, dQ=None, dK=None,
+                      dV=None, stream=None):
+    """dQ, dK, dV in one launch from a workspace fa_backward_preprocess filled."""
+    B, H, n, d = Q.shape
+    m = K.shape[2]
+    dQ = torch.empty_like(Q) if dQ is None else dQ
+    dK = torch.empty_like(K) if dK is None else dK
+    dV = torch.empty_like(V) if dV is None else dV
+    rc = lib().fa_backward_grads(Q.data_ptr(), K.data_ptr(), V.data_ptr(), dO.data_ptr(), B, H,
+                                 n, m, d, int(bool(causal)), _scale(scale, d), dQ.data_ptr(),
+                                 dK.data_ptr(), dV.data_ptr(), workspace.data_ptr(),
+                                 workspace.numel(), _stream(Q, stream))
+    _check("fa_backward_grads", rc)
+    return dQ, dK, dV
 
 
 def fa_get_device_status() -> int:

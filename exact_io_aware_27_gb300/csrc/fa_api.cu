@@ -282,6 +282,17 @@ int fa_backward_dq(const void* Q, const void* K, const void* V, const void* dO, 
   return from_cuda(launch_bwd_dq(a, static_cast<cudaStream_t>(stream)));
 }
 
+int fa_backward_grads(const void* Q, const void* K, const void* V, const void* dO, int B, int H,
+                      int n, int m, int d, int causal, float scale, void* dQ, void* dK, void* dV,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+  if (!Q || !K || !V || !dO || !dQ || !dK || !dV) return FA_ERR_INVALID_ARG;
+  BwdArgs a;
+  const int rc = prepare_backward(Q, K, V, nullptr, nullptr, dO, B, H, n, m, d, causal, scale,
+                                  dQ, dK, dV, workspace, workspace_bytes, false, false, &a);
+  if (rc != FA_OK) return rc;
+  return from_cuda(launch_bwd_main(a, static_cast<cudaStream_t>(stream)));
+}
+
 int fa_backward(const void* Q, const void* K, const void* V, const void* O, const float* L,
                 const void* dO, int B, int H, int n, int m, int d, int causal, float scale,
                 void* dQ, void* dK, void* dV, void* workspace, size_t workspace_bytes,
@@ -292,8 +303,7 @@ int fa_backward(const void* Q, const void* K, const void* V, const void* O, cons
   if (rc != FA_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_bwd_preprocess(a, s);
-  if (e == cudaSuccess) e = launch_bwd_dkdv(a, s);
-  if (e == cudaSuccess) e = launch_bwd_dq(a, s);
+  if (e == cudaSuccess) e = launch_bwd_main(a, s);
   return from_cuda(e);
 }
 

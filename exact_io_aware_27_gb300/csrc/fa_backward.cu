@@ -160,10 +160,13 @@ struct KvCfg {
   static constexpr int B_QE = B_QF + STAGES;  // + stage: the block's products done
   static constexpr int B_SF = B_QE + STAGES;  // + region: S^T in that region done
   static constexpr int B_DPF = B_SF + 2;      // dP^T of the current half done
-  static constexpr int B_PF = B_SF + 3;       // P^T in TMEM (256 arrivals)
-  static constexpr int B_DSF = B_SF + 4;      // dS^T in TMEM (256 arrivals)
-  static constexpr int B_ACC = B_SF + 5;      // dK, dV final
-  static constexpr int B_DRAIN = B_SF + 6;
+  // + (u & 1): P^T of half u in TMEM (256 arrivals). Two slots: P^T of half u+1
+  // needs only S^T_{u+1}, which is issued before the MMA warp waits for P^T_u,
+  // so one barrier could complete twice before that wait and hide its phase.
+  static constexpr int B_PF = B_SF + 3;
+  static constexpr int B_DSF = B_SF + 5;      // dS^T in TMEM (256 arrivals)
+  static constexpr int B_ACC = B_SF + 6;      // dK, dV final
+  static constexpr int B_DRAIN = B_SF + 7;
   static constexpr int NBAR = B_DRAIN + 1;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;
   // TMEM columns: K as bf16 pairs, two 64-column S^T regions, the dP^T region,
@@ -193,12 +196,12 @@ __device__ __forceinline__ uint32_t half_operand_col(uint32_t reg, int part, int
   return reg + (uint32_t)((kk >> 1) * 32 + part * 16 + (kk & 1) * 8);
 }
 
+// One CTA of the dK, dV pass: key block `lin` in launch order.
 template <int D>
-__global__ void __launch_bounds__(384, 1)
-    dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                const __grid_constant__ CUtensorMap tmNL2, const __grid_constant__ CUtensorMap tmND,
-                const KvParams p) {
+__device__ __forceinline__ void dkdv_cta(const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                                         const CUtensorMap& tmV, const CUtensorMap& tmdO,
+                                         const CUtensorMap& tmNL2, const CUtensorMap& tmND,
+                                         const KvParams& p, int lin) {
   using C = KvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -212,7 +215,7 @@ __global__ void __launch_bounds__(384, 1)
   // Key blocks near 0 carry the most work under causal masking: rank 0 first,
   // heads taken a group at a time so the blocks in flight share L2.
   int ktile, bh;
-  grouped_tile(blockIdx.x, p.BH, p.ktiles, p.group, ktile, bh);
+  grouped_tile(lin, p.BH, p.ktiles, p.group, ktile, bh);
   const int ks = ktile * C::BN;
   const int nqb = (p.n + C::BQ - 1) / C::BQ;
   const int i_start = p.causal ? ks / C::BQ : 0;  // first block with a query q >= ks
@@ -230,6 +233,7 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(&bar[C::B_SF + 1], 1);
     mbar_init(&bar[C::B_DPF], 1);
     mbar_init(&bar[C::B_PF], C::COMPUTE_THREADS);
+    mbar_init(&bar[C::B_PF + 1], C::COMPUTE_THREADS);
     mbar_init(&bar[C::B_DSF], C::COMPUTE_THREADS);
     mbar_init(&bar[C::B_ACC], 1);
     mbar_init(&bar[C::B_DRAIN], 1);
@@ -334,7 +338,7 @@ __global__ void __launch_bounds__(384, 1)
         if (nu > 1) scores(1);
       }
       for (int u = 0; ok && u < nu; ++u) {
-        if (!warp_wait(&bar[C::B_PF], u & 1, wc)) break;
+        if (!warp_wait(&bar[C::B_PF + (u & 1)], (u >> 1) & 1, wc)) break;
         tc_fence_after();
         grads(u, 0);
         if (!warp_wait(&bar[C::B_DSF], u & 1, wc)) break;
@@ -418,7 +422,7 @@ __global__ void __launch_bounds__(384, 1)
       tmem_st16(sr_col, pp);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bar[C::B_PF]);
+      mbar_arrive(&bar[C::B_PF + h]);
       if (!warp_wait(&bar[C::B_DPF], u & 1, wc)) { ok = false; break; }
       tc_fence_after();
       uint32_t dr[32], ws[16];
@@ -527,11 +531,11 @@ struct DqParams {
   float scale, scale_log2;
 };
 
+// One CTA of the dQ pass: query block `lin` in launch order.
 template <int D>
-__global__ void __launch_bounds__(384, 1)
-    dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-              const DqParams p) {
+__device__ __forceinline__ void dq_cta(const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                                       const CUtensorMap& tmV, const CUtensorMap& tmdO,
+                                       const DqParams& p, int lin) {
   using C = QCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -544,7 +548,7 @@ __global__ void __launch_bounds__(384, 1)
   const int lane = threadIdx.x & 31;
   // Under causal masking the last query blocks see the most keys: they go first.
   int rank, bh;
-  grouped_tile(blockIdx.x, p.BH, p.qtiles, p.group, rank, bh);
+  grouped_tile(lin, p.BH, p.qtiles, p.group, rank, bh);
   const int qtile = p.causal ? p.qtiles - 1 - rank : rank;
   const int q0 = qtile * C::BM;
   int nkb = (p.m + C::BN - 1) / C::BN;
@@ -833,64 +837,67 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const __nv_bfloat16* __
   }
 }
 
+// The dK, dV and dQ passes in one launch: n_kv CTAs of the first, then n_dq of
+// the second, whose heavy blocks fill the SMs the first pass's tail leaves idle.
 template <int D>
-cudaError_t launch_dkdv_d(const BwdArgs& a, cudaStream_t stream) {
-  using C = KvCfg<D>;
-  CUtensorMap mq, mk, mv, mdo, ml2, md;
-  if (make_bf16_head_map(&mq, a.Q, a.BH, a.n, D, C::BQ) != CUDA_SUCCESS ||
-      make_bf16_head_map(&mk, a.K, a.BH, a.m, D, C::BN) != CUDA_SUCCESS ||
-      make_bf16_head_map(&mv, a.V, a.BH, a.m, D, C::BN) != CUDA_SUCCESS ||
-      make_bf16_head_map(&mdo, a.dO, a.BH, a.n, D, C::BQ) != CUDA_SUCCESS ||
-      make_f32_row_map(&ml2, a.ws_nL2, a.BH, a.n_pad, C::BQ) != CUDA_SUCCESS ||
-      make_f32_row_map(&md, a.ws_nD, a.BH, a.n_pad, C::BQ) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
-  KvParams p;
-  p.dK = static_cast<__nv_bfloat16*>(a.dK);
-  p.dV = static_cast<__nv_bfloat16*>(a.dV);
-  p.n = a.n;
-  p.m = a.m;
-  p.n_pad = a.n_pad;
-  p.BH = a.BH;
-  p.causal = a.causal;
-  p.scale = a.scale;
-  p.scale_log2 = a.scale * kLog2e;
-  p.ktiles = ceil_div(a.m, C::BN);
-  p.group = heads_per_group(a.BH, p.ktiles);
-  cudaError_t e =
-      cudaFuncSetAttribute(dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-  if (e != cudaSuccess) return e;
-  const unsigned grid = (unsigned)p.ktiles * (unsigned)a.BH;
-  dkdv_kernel<D><<<grid, C::THREADS, C::SMEM, stream>>>(mq, mk, mv, mdo, ml2, md, p);
-  return cudaGetLastError();
+__global__ void __launch_bounds__(384, 1)
+    bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+               const __grid_constant__ CUtensorMap tmNL2, const __grid_constant__ CUtensorMap tmND,
+               const KvParams kp, const DqParams qp, int n_kv, int n_dq) {
+  const int b = blockIdx.x;
+  if (b < n_kv)
+    dkdv_cta<D>(tmQ, tmK, tmV, tmdO, tmNL2, tmND, kp, b);
+  else
+    dq_cta<D>(tmQ, tmK, tmV, tmdO, qp, b - n_kv);
 }
 
 template <int D>
-cudaError_t launch_dq_d(const BwdArgs& a, cudaStream_t stream) {
-  using C = QCfg<D>;
-  CUtensorMap mq, mk, mv, mdo;
-  if (make_bf16_head_map(&mq, a.Q, a.BH, a.n, D, C::BM) != CUDA_SUCCESS ||
-      make_bf16_head_map(&mk, a.K, a.BH, a.m, D, C::BN) != CUDA_SUCCESS ||
-      make_bf16_head_map(&mv, a.V, a.BH, a.m, D, C::BN) != CUDA_SUCCESS ||
-      make_bf16_head_map(&mdo, a.dO, a.BH, a.n, D, C::BM) != CUDA_SUCCESS)
+cudaError_t launch_bwd_d(const BwdArgs& a, bool with_kv, bool with_dq, cudaStream_t stream) {
+  using KC = KvCfg<D>;
+  using QC = QCfg<D>;
+  static_assert(KC::BQ == QC::BM && KC::BN == QC::BN, "the passes share the tensor maps");
+  CUtensorMap mq, mk, mv, mdo, ml2, md;
+  if (make_bf16_head_map(&mq, a.Q, a.BH, a.n, D, KC::BQ) != CUDA_SUCCESS ||
+      make_bf16_head_map(&mk, a.K, a.BH, a.m, D, KC::BN) != CUDA_SUCCESS ||
+      make_bf16_head_map(&mv, a.V, a.BH, a.m, D, KC::BN) != CUDA_SUCCESS ||
+      make_bf16_head_map(&mdo, a.dO, a.BH, a.n, D, KC::BQ) != CUDA_SUCCESS ||
+      make_f32_row_map(&ml2, a.ws_nL2, a.BH, a.n_pad, KC::BQ) != CUDA_SUCCESS ||
+      make_f32_row_map(&md, a.ws_nD, a.BH, a.n_pad, KC::BQ) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  DqParams p;
-  p.dQ = static_cast<__nv_bfloat16*>(a.dQ);
-  p.nD = a.ws_nD;
-  p.nL2 = a.ws_nL2;
-  p.n = a.n;
-  p.m = a.m;
-  p.n_pad = a.n_pad;
-  p.BH = a.BH;
-  p.causal = a.causal;
-  p.scale = a.scale;
-  p.scale_log2 = a.scale * kLog2e;
-  p.qtiles = ceil_div(a.n, C::BM);
-  p.group = heads_per_group(a.BH, p.qtiles);
+  KvParams kp;
+  kp.dK = static_cast<__nv_bfloat16*>(a.dK);
+  kp.dV = static_cast<__nv_bfloat16*>(a.dV);
+  kp.n = a.n;
+  kp.m = a.m;
+  kp.n_pad = a.n_pad;
+  kp.BH = a.BH;
+  kp.causal = a.causal;
+  kp.scale = a.scale;
+  kp.scale_log2 = a.scale * kLog2e;
+  kp.ktiles = ceil_div(a.m, KC::BN);
+  kp.group = heads_per_group(a.BH, kp.ktiles);
+  DqParams qp;
+  qp.dQ = static_cast<__nv_bfloat16*>(a.dQ);
+  qp.nD = a.ws_nD;
+  qp.nL2 = a.ws_nL2;
+  qp.n = a.n;
+  qp.m = a.m;
+  qp.n_pad = a.n_pad;
+  qp.BH = a.BH;
+  qp.causal = a.causal;
+  qp.scale = a.scale;
+  qp.scale_log2 = a.scale * kLog2e;
+  qp.qtiles = ceil_div(a.n, QC::BM);
+  qp.group = heads_per_group(a.BH, qp.qtiles);
+  const int n_kv = with_kv ? kp.ktiles * a.BH : 0;
+  const int n_dq = with_dq ? qp.qtiles * a.BH : 0;
+  constexpr int smem = KC::SMEM > QC::SMEM ? KC::SMEM : QC::SMEM;
   cudaError_t e =
-      cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+      cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const unsigned grid = (unsigned)p.qtiles * (unsigned)a.BH;
-  dq_kernel<D><<<grid, C::THREADS, C::SMEM, stream>>>(mq, mk, mv, mdo, p);
+  bwd_kernel<D><<<(unsigned)(n_kv + n_dq), KC::THREADS, smem, stream>>>(mq, mk, mv, mdo, ml2, md,
+                                                                        kp, qp, n_kv, n_dq);
   return cudaGetLastError();
 }
 
@@ -918,11 +925,15 @@ cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t s) {
-  return a.d == 128 ? launch_dkdv_d<128>(a, s) : launch_dkdv_d<64>(a, s);
+  return a.d == 128 ? launch_bwd_d<128>(a, true, false, s) : launch_bwd_d<64>(a, true, false, s);
 }
 
 cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t s) {
-  return a.d == 128 ? launch_dq_d<128>(a, s) : launch_dq_d<64>(a, s);
+  return a.d == 128 ? launch_bwd_d<128>(a, false, true, s) : launch_bwd_d<64>(a, false, true, s);
+}
+
+cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t s) {
+  return a.d == 128 ? launch_bwd_d<128>(a, true, true, s) : launch_bwd_d<64>(a, true, true, s);
 }
 
 cudaError_t bwd_read_status(unsigned int* out) {

@@ -57,6 +57,8 @@ cudaError_t launch_forward(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t s);
+// dK, dV and dQ in one launch (the two passes' CTAs interleaved).
+cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t s);
 
 // Read-and-clear of each translation unit's device status word.
 cudaError_t forward_read_status(unsigned int* out);

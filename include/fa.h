@@ -86,8 +86,8 @@ FA_API size_t fa_backward_workspace_size(int B, int H, int n, int m, int d);
  * FlashAttention-2 recompute form). Inputs Q, K, V, the forward's O and L, and
  * dO. Outputs dQ [B,H,n,d], dK and dV [B,H,m,d] (bf16). `workspace` is caller
  * owned device memory of at least fa_backward_workspace_size() bytes; its
- * contents on entry do not matter. Queues fa_backward_preprocess,
- * fa_backward_dkdv and fa_backward_dq on `stream`, in that order.
+ * contents on entry do not matter. Queues fa_backward_preprocess and
+ * fa_backward_grads on `stream`, in that order.
  */
 FA_API int fa_backward(const void* Q, const void* K, const void* V, const void* O, const float* L,
                 const void* dO, int B, int H, int n, int m, int d, int causal, float scale,
@@ -109,6 +109,9 @@ FA_API int fa_backward(const void* Q, const void* K, const void* V, const void* 
  *   accumulate dQ = dS K * scale on chip and write it once (the pages add dS K
  *   into dQ from inside the key loop; this computes the same sum as its own
  *   pass, with no read-modify-write of dQ in memory).
+ * fa_backward_grads: fa_backward_dkdv and fa_backward_dq as one kernel launch
+ *   (their thread blocks interleaved); what fa_backward queues after the
+ *   preprocess stage. Results are bitwise identical to the two separate calls.
  */
 FA_API int fa_backward_preprocess(const void* O, const void* dO, const float* L, int B, int H, int n,
                            int d, void* workspace, size_t workspace_bytes, void* stream);
@@ -118,6 +121,10 @@ FA_API int fa_backward_dkdv(const void* Q, const void* K, const void* V, const v
 FA_API int fa_backward_dq(const void* Q, const void* K, const void* V, const void* dO, int B, int H,
                    int n, int m, int d, int causal, float scale, void* dQ, void* workspace,
                    size_t workspace_bytes, void* stream);
+FA_API int fa_backward_grads(const void* Q, const void* K, const void* V, const void* dO, int B,
+                             int H, int n, int m, int d, int causal, float scale, void* dQ,
+                             void* dK, void* dV, void* workspace, size_t workspace_bytes,
+                             void* stream);
 
 /*
  * Backward pass without a caller-supplied workspace (the pages have no

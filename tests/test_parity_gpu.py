@@ -232,8 +232,10 @@ def test_stage_entry_points_match_fa_backward():
     fa.fa_backward_preprocess(O, dO, L, ws)
     dQ2 = fa.fa_backward_dq(Q, K, V, dO, ws, causal=True)  # either order after preprocess
     dK2, dV2 = fa.fa_backward_dkdv(Q, K, V, dO, ws, causal=True)
+    dQ3, dK3, dV3 = fa.fa_backward_grads(Q, K, V, dO, ws, causal=True)
     torch.cuda.synchronize()
     assert torch.equal(dK, dK2) and torch.equal(dV, dV2) and torch.equal(dQ, dQ2)
+    assert torch.equal(dK, dK3) and torch.equal(dV, dV3) and torch.equal(dQ, dQ3)
 
 
 def test_repeatable_and_no_timeout():
