@@ -131,44 +131,52 @@ __device__ __forceinline__ void dscores32(const uint32_t* p, const uint32_t* dp,
 }
 
 // ================================================================== dK, dV
-// K of the key block is moved into TMEM once (the A operand of S^T); V stays in
-// shared memory. Each query block is taken in two halves of 64 queries and both
+// One CTA walks a list of key blocks (persistent). For each block, K is moved into
+// TMEM (the A operand of S^T) and V stays in shared memory (two buffers,
+// alternating between blocks). The query loop runs in halves of 64 queries; both
 // compute groups work on every half (32 queries each). S^T of consecutive halves
-// alternates between two TMEM regions and dP^T has a region of its own, so S^T
-// of half u+2 is formed while half u is still being processed:
+// alternates between two TMEM regions and dP^T has a region of its own, so S^T of
+// half u+2 is formed while half u is processed:
 //   S^T_0 dP^T_0 S^T_1 | dV_0 dP^T_1 dK_0 S^T_2 | dV_1 dP^T_2 dK_1 S^T_3 | ...
+// Q, dO, -L2 and -D stream through a ring of half-block slots (64 queries each);
+// the next key block's K comes through the same ring (one slot) and its V into the
+// other V buffer while the current block runs; dK, dV are written out while the
+// next block's first products run.
 template <int D>
 struct KvCfg {
-  static constexpr int BN = 128;      // keys per CTA = TMEM lanes
+  static constexpr int BN = 128;      // keys per block = TMEM lanes
   static constexpr int BQ = 128;      // queries per block (two halves of 64)
   static constexpr int KCH = D / 64;  // 128-byte column chunks of a row
   static constexpr int CHUNK = 128 * 128;
-  static constexpr int TILE = KCH * CHUNK;       // 128 rows of Q, dO, K or V
-  static constexpr int HALF_ROWS = 64 * 128;     // bytes of 64 rows of one chunk
-  static constexpr int STAGES = (D == 128) ? 2 : 4;
-  static constexpr int K_STAGE = STAGES - 1;     // its Q buffer holds K until K is in TMEM
-  static constexpr int OFF_V = 0;
-  static constexpr int OFF_Q = TILE;
-  static constexpr int OFF_DO = OFF_Q + STAGES * TILE;
-  static constexpr int OFF_NL2 = OFF_DO + STAGES * TILE;     // [STAGES][BQ] fp32
-  static constexpr int OFF_ND = OFF_NL2 + STAGES * BQ * 4;   // [STAGES][BQ] fp32
-  static constexpr int OFF_BAR = OFF_ND + STAGES * BQ * 4;
+  static constexpr int TILE = KCH * CHUNK;       // 128 rows of K or V
+  static constexpr int HCHUNK = 64 * 128;        // one chunk of a 64-row tile
+  static constexpr int HTILE = KCH * HCHUNK;     // 64 rows of Q or dO
+  // Ring of half-block slots: Q (HTILE) then dO (HTILE) of 64 queries, or the next
+  // key block's K (TILE = 2 HTILE) in one slot.
+  static constexpr int SLOT = 2 * HTILE;
+  static constexpr int STAGES = (D == 128) ? 4 : 8;
+  static constexpr int OFF_V = 0;                // two V buffers
+  static constexpr int OFF_R = 2 * TILE;         // the ring
+  static constexpr int OFF_NL2 = OFF_R + STAGES * SLOT;      // [STAGES][64] fp32
+  static constexpr int OFF_ND = OFF_NL2 + STAGES * 64 * 4;   // [STAGES][64] fp32
+  static constexpr int OFF_BAR = OFF_ND + STAGES * 64 * 4;
   // barrier slots
-  static constexpr int B_KV = 0;              // K, V landed in shared memory
-  static constexpr int B_IN = 1;              // K in TMEM (256 arrivals)
-  static constexpr int B_QF = 2;              // + stage: Q_i, dO_i, -L2_i, -D_i landed
-  static constexpr int B_QE = B_QF + STAGES;  // + stage: the block's products done
-  static constexpr int B_SF = B_QE + STAGES;  // + region: S^T in that region done
+  static constexpr int B_QF = 0;              // + slot: the slot's copies landed
+  static constexpr int B_QE = STAGES;         // + slot: the slot may be refilled
+  static constexpr int B_VF = 2 * STAGES;     // + buffer: V landed
+  static constexpr int B_IN = B_VF + 2;       // K in TMEM (256 arrivals)
+  static constexpr int B_SF = B_IN + 1;       // + region: S^T in that region done
   static constexpr int B_DPF = B_SF + 2;      // dP^T of the current half done
   // + (u & 1): P^T of half u in TMEM (256 arrivals). Two slots: P^T of half u+1
   // needs only S^T_{u+1}, which is issued before the MMA warp waits for P^T_u,
   // so one barrier could complete twice before that wait and hide its phase.
   static constexpr int B_PF = B_SF + 3;
   static constexpr int B_DSF = B_SF + 5;      // dS^T in TMEM (256 arrivals)
-  static constexpr int B_ACC = B_SF + 6;      // dK, dV final
-  static constexpr int B_DRAIN = B_SF + 7;
+  static constexpr int B_ACC = B_SF + 6;      // + (block & 1): dK, dV final
+  static constexpr int B_EPI = B_SF + 8;      // dK, dV read out of TMEM (256 arrivals)
+  static constexpr int B_DRAIN = B_SF + 9;
   static constexpr int NBAR = B_DRAIN + 1;
-  static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;
+  static constexpr int SMEM = OFF_BAR + NBAR * 8 + 1024;
   // TMEM columns: K as bf16 pairs, two 64-column S^T regions, the dP^T region,
   // dV, dK. Group w keeps P^T over [32w, 32w + 16) and dS^T over
   // [32w + 16, 32w + 32) of the half's S^T region.
@@ -177,11 +185,11 @@ struct KvCfg {
   static constexpr uint32_t COL_DP = 192;
   static constexpr uint32_t COL_DV = 256;
   static constexpr uint32_t COL_DK = 256 + D;
-  static constexpr uint32_t TMEM_COLS = 512;
   static constexpr int THREADS = 384;
   static constexpr int COMPUTE_THREADS = 256;
-  static_assert(COL_DK + D <= TMEM_COLS, "TMEM budget");
-  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(COL_DK + D <= 512, "TMEM budget");
+  static_assert(SMEM <= 232448 - 64, "shared memory budget");
+  static_assert(SLOT == TILE, "a slot holds one K tile");
 };
 
 struct KvParams {
@@ -190,120 +198,196 @@ struct KvParams {
   float scale, scale_log2;
 };
 
+// Item of round r for CTA c of P in the persistent schedule: rounds alternate their
+// direction so that, with the items in heaviest-first order, every CTA gets about
+// the same total work.
+__device__ __forceinline__ int snake_item(int r, int c, int P) {
+  return r * P + ((r & 1) ? P - 1 - c : c);
+}
+
 // TMEM column of k-step kk (16 queries) of the P^T (part 0) or dS^T (part 1)
 // operand of a half stored in region `reg`.
 __device__ __forceinline__ uint32_t half_operand_col(uint32_t reg, int part, int kk) {
   return reg + (uint32_t)((kk >> 1) * 32 + part * 16 + (kk & 1) * 8);
 }
 
-// One CTA of the dK, dV pass: key block `lin` in launch order.
+// Copies row `r` of a 128-row, 128-byte-swizzled bf16 tile (D / 64 chunks) into
+// TMEM columns [col, col + D/2) of this thread's lane: piece j of a chunk row sits
+// at j ^ (r % 8).
 template <int D>
-__device__ __forceinline__ void dkdv_cta(const CUtensorMap& tmQ, const CUtensorMap& tmK,
+__device__ __forceinline__ void tile_row_to_tmem(const uint8_t* tile, int r, uint32_t col) {
+#pragma unroll
+  for (int c = 0; c < D / 64; ++c) {
+    uint32_t v[32];
+    const uint8_t* row = tile + c * (128 * 128) + r * 128;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint4 x = *reinterpret_cast<const uint4*>(row + ((j ^ (r & 7)) << 4));
+      v[4 * j] = x.x;
+      v[4 * j + 1] = x.y;
+      v[4 * j + 2] = x.z;
+      v[4 * j + 3] = x.w;
+    }
+    tmem_st32(col + 32 * c, v);
+  }
+  tmem_st_wait();
+}
+
+// Rows [r0, ...) of a TMEM accumulator (this thread's lane), scaled and stored as a
+// bf16 row of D values at dst (skipped when !store).
+template <int D, int NCOL>
+__device__ __forceinline__ void tmem_row_out(uint32_t col, float mul, __nv_bfloat16* dst,
+                                             bool store) {
+#pragma unroll
+  for (int c = 0; c < NCOL / 32; ++c) {
+    uint32_t o[32];
+    tmem_ld32(col + 32 * c, o);
+    tmem_ld_wait();
+    reg_fence32(o);
+    uint32_t wv[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      wv[e] = pack_bf16(__uint_as_float(o[2 * e]) * mul, __uint_as_float(o[2 * e + 1]) * mul);
+    if (store) {
+      uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+      d4[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+      d4[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
+      d4[2] = make_uint4(wv[8], wv[9], wv[10], wv[11]);
+      d4[3] = make_uint4(wv[12], wv[13], wv[14], wv[15]);
+    }
+  }
+}
+
+// Key blocks snake_item(r0 + t, c, P) (t < count) in launch order, by CTA c.
+template <int D>
+__device__ __forceinline__ void dkdv_run(const CUtensorMap& tmQ, const CUtensorMap& tmK,
                                          const CUtensorMap& tmV, const CUtensorMap& tmdO,
                                          const CUtensorMap& tmNL2, const CUtensorMap& tmND,
-                                         const KvParams& p, int lin) {
+                                         const KvParams& p, uint8_t* smem, uint32_t tmem,
+                                         int r0, int c, int P, int count, const WaitCtx& wc) {
   using C = KvCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + C::NBAR);
-  volatile uint32_t* abort_flag = tmem_slot + 1;
-  const WaitCtx wc{abort_flag, &g_bwd_status};
-
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // Key blocks near 0 carry the most work under causal masking: rank 0 first,
-  // heads taken a group at a time so the blocks in flight share L2.
-  int ktile, bh;
-  grouped_tile(lin, p.BH, p.ktiles, p.group, ktile, bh);
-  const int ks = ktile * C::BN;
-  const int nqb = (p.n + C::BQ - 1) / C::BQ;
-  const int i_start = p.causal ? ks / C::BQ : 0;  // first block with a query q >= ks
-  const int nq = max(0, nqb - i_start);
-  const int nu = 2 * nq;                          // halves
-
   if (threadIdx.x == 0) {
-    mbar_init(&bar[C::B_KV], 1);
-    mbar_init(&bar[C::B_IN], C::COMPUTE_THREADS);
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&bar[C::B_QF + s], 1);
       mbar_init(&bar[C::B_QE + s], 1);
     }
-    mbar_init(&bar[C::B_SF], 1);
-    mbar_init(&bar[C::B_SF + 1], 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bar[C::B_VF + b], 1);
+      mbar_init(&bar[C::B_SF + b], 1);
+      mbar_init(&bar[C::B_PF + b], C::COMPUTE_THREADS);
+      mbar_init(&bar[C::B_ACC + b], 1);
+    }
+    mbar_init(&bar[C::B_IN], C::COMPUTE_THREADS);
     mbar_init(&bar[C::B_DPF], 1);
-    mbar_init(&bar[C::B_PF], C::COMPUTE_THREADS);
-    mbar_init(&bar[C::B_PF + 1], C::COMPUTE_THREADS);
     mbar_init(&bar[C::B_DSF], C::COMPUTE_THREADS);
-    mbar_init(&bar[C::B_ACC], 1);
+    mbar_init(&bar[C::B_EPI], C::COMPUTE_THREADS);
     mbar_init(&bar[C::B_DRAIN], 1);
-    *abort_flag = 0u;
     fence_mbar_init();
   }
-  if (warp == 1) {
-    tmem_alloc(tmem_slot, C::TMEM_COLS);
-    tmem_relinquish();
-  }
-  tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  // Block t: first key, head, first query block and number of query blocks. Key
+  // blocks near 0 carry the most work under causal masking: the launch order puts
+  // rank 0 first, heads a group at a time so that the blocks in flight share L2.
+  auto block = [&](int t, int& ks, int& bh, int& i0, int& nq) {
+    int ktile;
+    grouped_tile(snake_item(r0 + t, c, P), p.BH, p.ktiles, p.group, ktile, bh);
+    ks = ktile * C::BN;
+    i0 = p.causal ? ks / C::BQ : 0;  // first query block with a query q >= ks
+    nq = max(0, (p.n + C::BQ - 1) / C::BQ - i0);
+  };
+  // Ring uses: per block one for its K, then one per query block. `ru` counts them,
+  // `hu` the halves and `at` the blocks with work, identically in every role.
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && nq > 0) {
+    if (lane == 0) {
       tma_prefetch_map(&tmQ);
       tma_prefetch_map(&tmK);
       tma_prefetch_map(&tmV);
       tma_prefetch_map(&tmdO);
-      mbar_arrive_expect_tx(&bar[C::B_KV], 2 * C::TILE);
-#pragma unroll
-      for (int c = 0; c < C::KCH; ++c) {
-        tma_load_3d(smem + C::OFF_Q + C::K_STAGE * C::TILE + c * C::CHUNK, &tmK, &bar[C::B_KV],
-                    c * 64, ks, bh);
-        tma_load_3d(smem + C::OFF_V + c * C::CHUNK, &tmV, &bar[C::B_KV], c * 64, ks, bh);
-      }
-      int issued = 0;
-      for (int i = 0; i < nq; ++i) {
-        const int s = i % C::STAGES;
-        const int q0 = (i_start + i) * C::BQ;
-        if (i >= C::STAGES && !mbar_wait(&bar[C::B_QE + s], ((i / C::STAGES) & 1) ^ 1, wc)) break;
-        if (i == C::K_STAGE && !mbar_wait(&bar[C::B_IN], 0, wc)) break;
-        uint64_t* f = &bar[C::B_QF + s];
-        mbar_arrive_expect_tx(f, 2 * C::TILE + 2 * C::BQ * 4);
+      int ru = 0, at = 0;
+      bool ok = true;
+      for (int t = 0; ok && t < count; ++t) {
+        int ks, bh, i0, nq;
+        block(t, ks, bh, i0, nq);
+        if (nq == 0) continue;
+        // V into buffer at % 2, free once block at-2's products are done
+        const int vb = at & 1;
+        if (at >= 2 && !mbar_wait(&bar[C::B_ACC + vb], ((at >> 1) & 1) ^ 1, wc)) break;
+        mbar_arrive_expect_tx(&bar[C::B_VF + vb], C::TILE);
 #pragma unroll
         for (int c = 0; c < C::KCH; ++c)
-          tma_load_3d(smem + C::OFF_Q + s * C::TILE + c * C::CHUNK, &tmQ, f, c * 64, q0, bh);
-        tma_load_2d(smem + C::OFF_NL2 + s * C::BQ * 4, &tmNL2, f, q0, bh);
-        tma_load_2d(smem + C::OFF_ND + s * C::BQ * 4, &tmND, f, q0, bh);
+          tma_load_3d(smem + C::OFF_V + vb * C::TILE + c * C::CHUNK, &tmV, &bar[C::B_VF + vb],
+                      c * 64, ks, bh);
+        for (int u = -1; u < 2 * nq; ++u, ++ru) {
+          const int s = ru % C::STAGES;
+          if (ru >= C::STAGES &&
+              !mbar_wait(&bar[C::B_QE + s], ((ru / C::STAGES) & 1) ^ 1, wc)) {
+            ok = false;
+            break;
+          }
+          uint64_t* f = &bar[C::B_QF + s];
+          uint8_t* slot = smem + C::OFF_R + s * C::SLOT;
+          if (u < 0) {  // this block's K
+            mbar_arrive_expect_tx(f, C::TILE);
 #pragma unroll
-        for (int c = 0; c < C::KCH; ++c)
-          tma_load_3d(smem + C::OFF_DO + s * C::TILE + c * C::CHUNK, &tmdO, f, c * 64, q0, bh);
-        issued = i + 1;
+            for (int c = 0; c < C::KCH; ++c)
+              tma_load_3d(slot + c * C::CHUNK, &tmK, f, c * 64, ks, bh);
+          } else {  // queries [q, q + 64) of half u: Q, dO, -L2, -D
+            const int q = (i0 + (u >> 1)) * C::BQ + 64 * (u & 1);
+            mbar_arrive_expect_tx(f, 2 * C::HTILE + 2 * 64 * 4);
+#pragma unroll
+            for (int c = 0; c < C::KCH; ++c) {
+              tma_load_3d(slot + c * C::HCHUNK, &tmQ, f, c * 64, q, bh);
+              tma_load_3d(slot + C::HTILE + c * C::HCHUNK, &tmdO, f, c * 64, q, bh);
+            }
+            tma_load_2d(smem + C::OFF_NL2 + s * 64 * 4, &tmNL2, f, q, bh);
+            tma_load_2d(smem + C::OFF_ND + s * 64 * 4, &tmND, f, q, bh);
+          }
+        }
+        if (ok) ++at;
       }
-      drain_wait(&bar[C::B_KV], 0);
-      for (int i = max(0, issued - C::STAGES); i < issued; ++i)
-        drain_wait(&bar[C::B_QF + i % C::STAGES], (i / C::STAGES) & 1);
+      // Let every copy this thread issued land before the run ends.
+      for (int r = max(0, ru - C::STAGES); r < ru; ++r)
+        drain_wait(&bar[C::B_QF + r % C::STAGES], (r / C::STAGES) & 1);
+      for (int a = max(0, at - 2); a < at; ++a) drain_wait(&bar[C::B_VF + (a & 1)], (a >> 1) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (nq > 0) {
-      constexpr uint32_t kIdescS = idesc_bf16_f32(128, 64, false, false);
-      constexpr uint32_t kIdescG = idesc_bf16_f32(128, D, false, true);
-      const uint64_t v_k = sdesc_sw128(smem_u32(smem + C::OFF_V), 16, 1024);  // V, K-major
-      auto sreg = [&](int u) { return tmem + C::COL_S + 64u * (uint32_t)(u & 1); };
-      // B operand rows of half u in the Q or dO buffer of its block
-      auto half_rows = [&](int base, int u) {
-        return smem_u32(smem + base + ((u >> 1) % C::STAGES) * C::TILE + (u & 1) * C::HALF_ROWS);
+    constexpr uint32_t kIdescS = idesc_bf16_f32(128, 64, false, false);
+    constexpr uint32_t kIdescG = idesc_bf16_f32(128, D, false, true);
+    auto sreg = [&](int u) { return tmem + C::COL_S + 64u * (uint32_t)(u & 1); };
+    int ru = 0, hu = 0, at = 0;
+    bool ok = true;
+    for (int t = 0; ok && t < count; ++t) {
+      int ks, bh, i0, nq;
+      block(t, ks, bh, i0, nq);
+      if (nq == 0) continue;
+      const int nu = 2 * nq;
+      const int rb = ru + 1;  // ring use of half 0
+      // K is in TMEM (its slot may be refilled), V landed, halves 0 and 1 landed
+      if (!warp_wait(&bar[C::B_IN], at & 1, wc)) break;
+      if (lane == 0) mbar_arrive(&bar[C::B_QE + ru % C::STAGES]);
+      if (!warp_wait(&bar[C::B_VF + (at & 1)], (at >> 1) & 1, wc)) break;
+      if (!warp_wait(&bar[C::B_QF + rb % C::STAGES], (rb / C::STAGES) & 1, wc)) break;
+      if (!warp_wait(&bar[C::B_QF + (rb + 1) % C::STAGES], ((rb + 1) / C::STAGES) & 1, wc)) break;
+      tc_fence_after();
+      const uint64_t v_k = sdesc_sw128(smem_u32(smem + C::OFF_V + (at & 1) * C::TILE), 16, 1024);
+      // Q (part 0) or dO (part 1) of half u in its slot
+      auto half_rows = [&](int part, int u) {
+        return smem_u32(smem + C::OFF_R + ((rb + u) % C::STAGES) * C::SLOT + part * C::HTILE);
       };
       // S^T_u = K Q_u^T (TS, N = 64) into its region. The region still holds
       // P^T / dS^T of half u-2, read by dV / dK of that half, which this thread
       // issued earlier: tcgen05.mma instructions of one thread execute in order.
       auto scores = [&](int u) {
-        const uint64_t b_k = sdesc_sw128(half_rows(C::OFF_Q, u), 16, 1024);
+        const uint64_t b_k = sdesc_sw128(half_rows(0, u), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
+          const uint32_t off = (kk >> 2) * C::HCHUNK + (kk & 3) * 32;
           umma_ts_w(sreg(u), tmem + C::COL_K + kk * 8, sdesc_add(b_k, off), kIdescS, kk > 0);
         }
         umma_commit_w(&bar[C::B_SF + (u & 1)]);
@@ -311,217 +395,201 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tmQ, const CUtensorM
       // dP^T_u = V dO_u^T (SS, N = 64). The compute groups read dP^T_{u-1}
       // before signalling dS^T_{u-1}.
       auto dscores = [&](int u) {
-        const uint64_t b_k = sdesc_sw128(half_rows(C::OFF_DO, u), 16, 1024);
+        const uint64_t b_k = sdesc_sw128(half_rows(1, u), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
-          umma_ss_w(tmem + C::COL_DP, sdesc_add(v_k, off), sdesc_add(b_k, off), kIdescS, kk > 0);
+          umma_ss_w(tmem + C::COL_DP, sdesc_add(v_k, (kk >> 2) * C::CHUNK + (kk & 3) * 32),
+                    sdesc_add(b_k, (kk >> 2) * C::HCHUNK + (kk & 3) * 32), kIdescS, kk > 0);
         }
         umma_commit_w(&bar[C::B_DPF]);
       };
       // dV += P^T_u dO_u (part 0) or dK += dS^T_u Q_u (part 1), TS
       auto grads = [&](int u, int part) {
-        const uint64_t b_mn =
-            sdesc_sw128(half_rows(part == 0 ? C::OFF_DO : C::OFF_Q, u), C::CHUNK, 1024);
+        const uint64_t b_mn = sdesc_sw128(half_rows(part == 0 ? 1 : 0, u), C::HCHUNK, 1024);
         const uint32_t dcol = tmem + (part == 0 ? C::COL_DV : C::COL_DK);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           umma_ts_w(dcol, half_operand_col(sreg(u), part, kk), sdesc_add(b_mn, kk * 2048),
                     kIdescG, (u > 0 || kk > 0) ? 1u : 0u);
       };
-      bool ok = warp_wait(&bar[C::B_IN], 0, wc) && warp_wait(&bar[C::B_KV], 0, wc) &&
-                warp_wait(&bar[C::B_QF], 0, wc);
-      if (ok) {
-        tc_fence_after();
-        scores(0);
-        dscores(0);
-        if (nu > 1) scores(1);
-      }
+      scores(0);
+      dscores(0);
+      scores(1);
       for (int u = 0; ok && u < nu; ++u) {
-        if (!warp_wait(&bar[C::B_PF + (u & 1)], (u >> 1) & 1, wc)) break;
+        if (!warp_wait(&bar[C::B_PF + (u & 1)], ((hu >> 1) + (u >> 1)) & 1, wc)) { ok = false; break; }
+        // the previous block's dK, dV have been read out of TMEM
+        if (u == 0 && at >= 1 && !warp_wait(&bar[C::B_EPI], (at - 1) & 1, wc)) { ok = false; break; }
         tc_fence_after();
         grads(u, 0);
-        if (!warp_wait(&bar[C::B_DSF], u & 1, wc)) break;
+        if (!warp_wait(&bar[C::B_DSF], (hu + u) & 1, wc)) { ok = false; break; }
         tc_fence_after();
         if (u + 1 < nu) dscores(u + 1);
         grads(u, 1);
-        if (u & 1) umma_commit_w(&bar[C::B_QE + (u >> 1) % C::STAGES]);  // block's last reader
+        umma_commit_w(&bar[C::B_QE + (rb + u) % C::STAGES]);  // last reader of half u's slot
         if (u + 2 < nu) {
-          if (((u + 2) & 1) == 0) {
-            const int i2 = (u + 2) >> 1;
-            if (!warp_wait(&bar[C::B_QF + i2 % C::STAGES], (i2 / C::STAGES) & 1, wc)) break;
-            tc_fence_after();
-          }
+          const int r2 = rb + u + 2;
+          if (!warp_wait(&bar[C::B_QF + r2 % C::STAGES], (r2 / C::STAGES) & 1, wc)) { ok = false; break; }
+          tc_fence_after();
           scores(u + 2);
         }
       }
-      umma_commit_w(&bar[C::B_ACC]);
-      umma_commit_w(&bar[C::B_DRAIN]);
-      drain_wait(&bar[C::B_DRAIN], 0);
+      if (!ok) break;
+      umma_commit_w(&bar[C::B_ACC + (at & 1)]);
+      ru += 1 + 2 * nq;
+      hu += nu;
+      ++at;
     }
+    umma_commit_w(&bar[C::B_DRAIN]);
+    drain_wait(&bar[C::B_DRAIN], 0);
   } else if (warp >= 4) {
     // ------------------------------------------------------------ P^T, dS^T
     const int w = (warp - 4) >> 2;               // compute group
     const int krow = (warp & 3) * 32 + lane;     // key row = TMEM lane
-    const int kg = ks + krow;
     const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const float sl2 = p.scale_log2;
-    const bool key_ok = kg < p.m;
+    // Group 0 writes dV rows, group 1 dK rows (all D columns of its key row).
+    const uint32_t acc_col = tl + (w == 0 ? C::COL_DV : C::COL_DK);
+    const float acc_mul = w == 0 ? 1.f : p.scale;
+    __nv_bfloat16* const out = w == 0 ? p.dV : p.dK;
+    int ru = 0, hu = 0, at = 0;
+    int prev_bh = 0, prev_ks = 0;
     bool ok = true;
-    if (nq > 0) {
-      // Group 0 moves key row krow of K into TMEM: the row's 16-byte pieces in
-      // the 128-byte-swizzled tile (piece j of a chunk row at j ^ (row % 8)).
-      if (w == 0) {
-        ok = warp_wait(&bar[C::B_KV], 0, wc);
-        if (ok) {
-          const uint8_t* tile = smem + C::OFF_Q + C::K_STAGE * C::TILE;
-#pragma unroll
-          for (int c = 0; c < D / 64; ++c) {
-            uint32_t v[32];
-            const uint8_t* row = tile + c * C::CHUNK + krow * 128;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const uint4 x = *reinterpret_cast<const uint4*>(row + ((j ^ (krow & 7)) << 4));
-              v[4 * j] = x.x;
-              v[4 * j + 1] = x.y;
-              v[4 * j + 2] = x.z;
-              v[4 * j + 3] = x.w;
-            }
-            tmem_st32(tl + C::COL_K + 32 * c, v);
-          }
-          tmem_st_wait();
-          tc_fence_before();
-        }
-      }
-      mbar_arrive(&bar[C::B_IN]);
-    }
-    for (int u = 0; ok && u < nu; ++u) {
-      const int i = u >> 1, h = u & 1;
-      const int s = i % C::STAGES;
-      const int c0 = 64 * h + 32 * w;              // first query column of this group
-      const int q0 = (i_start + i) * C::BQ;
-      if (h == 0 && !warp_wait(&bar[C::B_QF + s], (i / C::STAGES) & 1, wc)) { ok = false; break; }
-      if (!warp_wait(&bar[C::B_SF + h], (u >> 1) & 1, wc)) { ok = false; break; }
+    // dK / dV of block a (head pbh, keys from pks) out of TMEM
+    auto epilogue = [&](int a, int pbh, int pks) {
+      if (!warp_wait(&bar[C::B_ACC + (a & 1)], (a >> 1) & 1, wc)) return false;
       tc_fence_after();
-      const uint32_t sr_col = tl + C::COL_S + 64u * (uint32_t)h + 32u * (uint32_t)w;
-      const float* nl2 = reinterpret_cast<const float*>(smem + C::OFF_NL2 + s * C::BQ * 4) + c0;
-      const float* nd = reinterpret_cast<const float*>(smem + C::OFF_ND + s * C::BQ * 4) + c0;
-      // Columns c < hide are masked: query q0 + c0 + c < key kg under causal
-      // masking, or all of them for a key past m.
-      const int hide = key_ok ? (p.causal ? kg - q0 - c0 : 0) : 32;
-      const bool masked = __any_sync(0xffffffffu, hide > 0);
-      uint32_t sr[32], pp[16];
-      tmem_ld32(sr_col, sr);
-      tmem_ld_wait();
-      reg_fence32(sr);
-      if (masked)
-        probabilities32<true>(sr, pp, sl2, nl2, 0.f, hide, true);
-      else
-        probabilities32<true>(sr, pp, sl2, nl2, 0.f, 0, false);
-      // P^T (bf16) over the first 16 of this group's 32 S^T columns, already read.
-      tmem_st16(sr_col, pp);
-      tmem_st_wait();
+      const int kg = pks + krow;
+      tmem_row_out<D, D>(acc_col, acc_mul, out + ((size_t)pbh * p.m + kg) * D, kg < p.m);
       tc_fence_before();
-      mbar_arrive(&bar[C::B_PF + h]);
-      if (!warp_wait(&bar[C::B_DPF], u & 1, wc)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t dr[32], ws[16];
-      tmem_ld32(tl + C::COL_DP + 32u * (uint32_t)w, dr);
-      tmem_ld_wait();
-      reg_fence32(dr);
-      dscores32<true>(sr, dr, ws, nd, 0.f);
-      tmem_st16(sr_col + 16, ws);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&bar[C::B_DSF]);
-    }
-
-    // ------------------------------------------------------------ dK, dV out
-    // Group 0 writes dV, group 1 writes dK (each all D columns of its rows).
-    if (ok) {
-      const uint32_t col = w == 0 ? C::COL_DV : C::COL_DK;
-      const float mul = w == 0 ? 1.f : p.scale;
-      __nv_bfloat16* dst_row = (w == 0 ? p.dV : p.dK) + ((size_t)bh * p.m + kg) * D;
-      if (nq == 0) {
+      mbar_arrive(&bar[C::B_EPI]);
+      return true;
+    };
+    for (int t = 0; ok && t < count; ++t) {
+      int ks, bh, i0, nq;
+      block(t, ks, bh, i0, nq);
+      const int kg = ks + krow;
+      const bool key_ok = kg < p.m;
+      if (nq == 0) {  // no query sees these keys: dK = dV = 0
         if (key_ok) {
           const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-          for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(dst_row)[c] = z;
+          for (int c = 0; c < D / 8; ++c)
+            reinterpret_cast<uint4*>(out + ((size_t)bh * p.m + kg) * D)[c] = z;
         }
-      } else if (warp_wait(&bar[C::B_ACC], 0, wc)) {
-        tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tl + col + 32 * c, o);
-          tmem_ld_wait();
-          reg_fence32(o);
-          uint32_t wv[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e)
-            wv[e] = pack_bf16(__uint_as_float(o[2 * e]) * mul, __uint_as_float(o[2 * e + 1]) * mul);
-          if (key_ok) {
-            uint4* dst = reinterpret_cast<uint4*>(dst_row + 32 * c);
-            dst[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-            dst[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
-            dst[2] = make_uint4(wv[8], wv[9], wv[10], wv[11]);
-            dst[3] = make_uint4(wv[12], wv[13], wv[14], wv[15]);
-          }
-        }
+        continue;
       }
+      // K of this block into TMEM. The previous block's S^T products, the only
+      // readers of these columns, are complete: both groups waited for all of them.
+      if (w == 0) {
+        const int s = ru % C::STAGES;
+        if (!warp_wait(&bar[C::B_QF + s], (ru / C::STAGES) & 1, wc)) { ok = false; break; }
+        tile_row_to_tmem<D>(smem + C::OFF_R + s * C::SLOT, krow, tl + C::COL_K);
+        tc_fence_before();
+      }
+      mbar_arrive(&bar[C::B_IN]);
+      // The previous block's dK, dV leave TMEM while this block's first products run.
+      if (at >= 1 && !epilogue(at - 1, prev_bh, prev_ks)) { ok = false; break; }
+      const int rb = ru + 1;
+      for (int u = 0; ok && u < 2 * nq; ++u) {
+        const int i = u >> 1, h = u & 1;
+        const int s = (rb + u) % C::STAGES;
+        const int c0 = 64 * h + 32 * w;            // first query column of this group
+        const int q0 = (i0 + i) * C::BQ;
+        if (!warp_wait(&bar[C::B_QF + s], ((rb + u) / C::STAGES) & 1, wc)) { ok = false; break; }
+        if (!warp_wait(&bar[C::B_SF + h], ((hu >> 1) + (u >> 1)) & 1, wc)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t sr_col = tl + C::COL_S + 64u * (uint32_t)h + 32u * (uint32_t)w;
+        const float* nl2 = reinterpret_cast<const float*>(smem + C::OFF_NL2 + s * 64 * 4) + 32 * w;
+        const float* nd = reinterpret_cast<const float*>(smem + C::OFF_ND + s * 64 * 4) + 32 * w;
+        // Columns c < hide are masked: query q0 + c0 + c < key kg under causal
+        // masking, or all of them for a key past m.
+        const int hide = key_ok ? (p.causal ? kg - q0 - c0 : 0) : 32;
+        const bool masked = __any_sync(0xffffffffu, hide > 0);
+        uint32_t sr[32], pp[16];
+        tmem_ld32(sr_col, sr);
+        tmem_ld_wait();
+        reg_fence32(sr);
+        if (masked)
+          probabilities32<true>(sr, pp, sl2, nl2, 0.f, hide, true);
+        else
+          probabilities32<true>(sr, pp, sl2, nl2, 0.f, 0, false);
+        // P^T (bf16) over the first 16 of this group's 32 S^T columns, already read.
+        tmem_st16(sr_col, pp);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bar[C::B_PF + h]);
+        if (!warp_wait(&bar[C::B_DPF], (hu + u) & 1, wc)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t dr[32], ws[16];
+        tmem_ld32(tl + C::COL_DP + 32u * (uint32_t)w, dr);
+        tmem_ld_wait();
+        reg_fence32(dr);
+        dscores32<true>(sr, dr, ws, nd, 0.f);
+        tmem_st16(sr_col + 16, ws);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bar[C::B_DSF]);
+      }
+      prev_bh = bh;
+      prev_ks = ks;
+      ru += 1 + 2 * nq;
+      hu += 2 * nq;
+      ++at;
     }
+    if (ok && at >= 1) epilogue(at - 1, prev_bh, prev_ks);
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, C::TMEM_COLS);
-  }
+  if (threadIdx.x == 0)
+    for (int b = 0; b < C::NBAR; ++b) mbar_inval(&bar[b]);
 }
 
 // ================================================================== dQ
+// One CTA walks a list of query blocks (persistent). For each block, Q and dO come
+// through the K/V ring (one slot) and are moved into TMEM (the A operands of
+// S = Q K^T and dP = dO V^T); K and V stream through the ring. Each 128-key block
+// is taken in halves of 64 keys, one per compute group:
+//   S_0 dP_0 S_1 dP_1 | dQ_0 S_0' dP_0' dQ_1 S_1' dP_1' | ...  (' = next key block)
+// dQ accumulates in TMEM and is written once, scaled, as bf16, while the next query
+// block's first products run.
 template <int D>
 struct QCfg {
-  static constexpr int BM = 128;      // queries per CTA = TMEM lanes
+  static constexpr int BM = 128;      // queries per block = TMEM lanes
   static constexpr int BN = 128;      // keys per step
   static constexpr int KCH = D / 64;
   static constexpr int CHUNK = 128 * 128;
   static constexpr int TILE = KCH * CHUNK;
+  static constexpr int HALF_ROWS = 64 * 128;  // bytes of 64 rows of one 128-byte chunk
   static constexpr int STAGES = (D == 128) ? 3 : 4;
-  static constexpr int OFF_K = 0;
-  static constexpr int OFF_V = STAGES * TILE;
+  static constexpr int OFF_K = 0;              // ring: K_j (or the next block's Q)
+  static constexpr int OFF_V = STAGES * TILE;  // ring: V_j (or the next block's dO)
   static constexpr int OFF_BAR = 2 * STAGES * TILE;
-  // Q and dO of the block are copied into the last stage's K and V buffers
-  // first; the compute groups move them into TMEM, then the stage holds K, V.
-  static constexpr int QDO_STAGE = STAGES - 1;
-  static constexpr int B_QDO = 0;              // Q and dO landed in shared memory
-  static constexpr int B_IN = 1;               // Q and dO rows in TMEM (256 arrivals)
-  static constexpr int B_KVF = 2;              // + stage: K_j, V_j landed
-  static constexpr int B_KVE = B_KVF + STAGES;  // + stage: dQ_j done, refill
+  static constexpr int B_KVF = 0;              // + slot: the slot's copies landed
+  static constexpr int B_KVE = STAGES;         // + slot: the slot may be refilled
+  static constexpr int B_IN = 2 * STAGES;      // Q and dO rows in TMEM (256 arrivals)
   // Per half h of the key block (two slots each):
-  static constexpr int B_SF = B_KVE + STAGES;  // + h: S_h done
+  static constexpr int B_SF = B_IN + 1;        // + h: S_h done
   static constexpr int B_DPF = B_SF + 2;       // + h: dP_h done
   static constexpr int B_DSF = B_SF + 4;       // + h: dS_h in TMEM (128 arrivals)
-  static constexpr int B_ACC = B_SF + 6;
-  static constexpr int B_DRAIN = B_SF + 7;
+  static constexpr int B_ACC = B_SF + 6;       // dQ final
+  static constexpr int B_EPI = B_SF + 7;       // dQ read out of TMEM (256 arrivals)
+  static constexpr int B_DRAIN = B_SF + 8;
   static constexpr int NBAR = B_DRAIN + 1;
-  static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;
-  // TMEM columns: Q and dO as bf16 pairs (the A operands of S and dP); for half h
-  // of the key block S_h at COL_S + 64h (then dS_h as bf16 pairs over its first
-  // 32 columns) and dP_h at COL_DP + 64h; dQ.
+  static constexpr int SMEM = OFF_BAR + NBAR * 8 + 1024;
+  // TMEM columns: Q and dO as bf16 pairs; for half h of the key block S_h at
+  // COL_S + 64h (then dS_h as bf16 pairs over its first 32 columns) and dP_h at
+  // COL_DP + 64h; dQ.
   static constexpr uint32_t COL_Q = 0;
   static constexpr uint32_t COL_DO = D / 2;
   static constexpr uint32_t COL_S = D;
   static constexpr uint32_t COL_DP = D + 128;
   static constexpr uint32_t COL_DQ = D + 256;
-  static constexpr uint32_t TMEM_COLS = 512;
   static constexpr int THREADS = 384;
   static constexpr int COMPUTE_THREADS = 256;
   static constexpr int GROUP_THREADS = 128;
-  static constexpr int HALF_ROWS = 64 * 128;  // bytes of 64 rows of one 128-byte chunk
-  static_assert(COL_DQ + D <= TMEM_COLS, "TMEM budget");
-  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(COL_DQ + D <= 512, "TMEM budget");
+  static_assert(SMEM <= 232448 - 64, "shared memory budget");
 };
 
 struct DqParams {
@@ -531,106 +599,103 @@ struct DqParams {
   float scale, scale_log2;
 };
 
-// One CTA of the dQ pass: query block `lin` in launch order.
+// Query blocks snake_item(r0 + t, c, P) - skip (t < count) in launch order, by CTA c.
 template <int D>
-__device__ __forceinline__ void dq_cta(const CUtensorMap& tmQ, const CUtensorMap& tmK,
+__device__ __forceinline__ void dq_run(const CUtensorMap& tmQ, const CUtensorMap& tmK,
                                        const CUtensorMap& tmV, const CUtensorMap& tmdO,
-                                       const DqParams& p, int lin) {
+                                       const DqParams& p, uint8_t* smem, uint32_t tmem, int r0,
+                                       int c, int P, int skip, int count, const WaitCtx& wc) {
   using C = QCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + C::NBAR);
-  volatile uint32_t* abort_flag = tmem_slot + 1;
-  const WaitCtx wc{abort_flag, &g_bwd_status};
-
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // Under causal masking the last query blocks see the most keys: they go first.
-  int rank, bh;
-  grouped_tile(lin, p.BH, p.qtiles, p.group, rank, bh);
-  const int qtile = p.causal ? p.qtiles - 1 - rank : rank;
-  const int q0 = qtile * C::BM;
-  int nkb = (p.m + C::BN - 1) / C::BN;
-  if (p.causal) nkb = min(nkb, min(q0 + C::BM - 1, p.n - 1) / C::BN + 1);  // keys k <= q
-
   if (threadIdx.x == 0) {
-    mbar_init(&bar[C::B_QDO], 1);
-    mbar_init(&bar[C::B_IN], C::COMPUTE_THREADS);
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&bar[C::B_KVF + s], 1);
       mbar_init(&bar[C::B_KVE + s], 1);
     }
+    mbar_init(&bar[C::B_IN], C::COMPUTE_THREADS);
     for (int h = 0; h < 2; ++h) {
       mbar_init(&bar[C::B_SF + h], 1);
       mbar_init(&bar[C::B_DPF + h], 1);
       mbar_init(&bar[C::B_DSF + h], C::GROUP_THREADS);
     }
     mbar_init(&bar[C::B_ACC], 1);
+    mbar_init(&bar[C::B_EPI], C::COMPUTE_THREADS);
     mbar_init(&bar[C::B_DRAIN], 1);
-    *abort_flag = 0u;
     fence_mbar_init();
   }
-  if (warp == 1) {
-    tmem_alloc(tmem_slot, C::TMEM_COLS);
-    tmem_relinquish();
-  }
-  tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  // Block t: head, first query, number of key blocks. Under causal masking the last
+  // query blocks see the most keys: the launch order puts them first.
+  auto block = [&](int t, int& bh, int& q0, int& nkb) {
+    int rank;
+    grouped_tile(snake_item(r0 + t, c, P) - skip, p.BH, p.qtiles, p.group, rank, bh);
+    q0 = (p.causal ? p.qtiles - 1 - rank : rank) * C::BM;
+    nkb = (p.m + C::BN - 1) / C::BN;
+    if (p.causal) nkb = min(nkb, min(q0 + C::BM - 1, p.n - 1) / C::BN + 1);  // keys k <= q
+  };
+  // Ring uses: per block one for its Q and dO, then one per key block. `ru` counts
+  // them, `gb` the key blocks and `at` the query blocks with work, in every role.
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && nkb > 0) {
+    if (lane == 0) {
       tma_prefetch_map(&tmQ);
       tma_prefetch_map(&tmK);
       tma_prefetch_map(&tmV);
       tma_prefetch_map(&tmdO);
-      {
-        uint64_t* f = &bar[C::B_QDO];
-        mbar_arrive_expect_tx(f, 2 * C::TILE);
+      int ru = 0;
+      bool ok = true;
+      for (int t = 0; ok && t < count; ++t) {
+        int bh, q0, nkb;
+        block(t, bh, q0, nkb);
+        if (nkb == 0) continue;
+        for (int j = -1; j < nkb; ++j, ++ru) {
+          const int s = ru % C::STAGES;
+          if (ru >= C::STAGES &&
+              !mbar_wait(&bar[C::B_KVE + s], ((ru / C::STAGES) & 1) ^ 1, wc)) {
+            ok = false;
+            break;
+          }
+          uint64_t* f = &bar[C::B_KVF + s];
+          mbar_arrive_expect_tx(f, 2 * C::TILE);
+          uint8_t* kb = smem + C::OFF_K + s * C::TILE;
+          uint8_t* vb = smem + C::OFF_V + s * C::TILE;
 #pragma unroll
-        for (int c = 0; c < C::KCH; ++c) {
-          tma_load_3d(smem + C::OFF_K + C::QDO_STAGE * C::TILE + c * C::CHUNK, &tmQ, f, c * 64,
-                      q0, bh);
-          tma_load_3d(smem + C::OFF_V + C::QDO_STAGE * C::TILE + c * C::CHUNK, &tmdO, f, c * 64,
-                      q0, bh);
+          for (int c = 0; c < C::KCH; ++c) {
+            if (j < 0) {  // this block's Q and dO (64-row boxes: rows q0 and q0 + 64)
+              tma_load_3d(kb + c * C::CHUNK, &tmQ, f, c * 64, q0, bh);
+              tma_load_3d(kb + c * C::CHUNK + C::HALF_ROWS, &tmQ, f, c * 64, q0 + 64, bh);
+              tma_load_3d(vb + c * C::CHUNK, &tmdO, f, c * 64, q0, bh);
+              tma_load_3d(vb + c * C::CHUNK + C::HALF_ROWS, &tmdO, f, c * 64, q0 + 64, bh);
+            } else {
+              tma_load_3d(kb + c * C::CHUNK, &tmK, f, c * 64, j * C::BN, bh);
+              tma_load_3d(vb + c * C::CHUNK, &tmV, f, c * 64, j * C::BN, bh);
+            }
+          }
         }
       }
-      int issued = 0;
-      for (int j = 0; j < nkb; ++j) {
-        const int s = j % C::STAGES;
-        if (j >= C::STAGES && !mbar_wait(&bar[C::B_KVE + s], ((j / C::STAGES) & 1) ^ 1, wc))
-          break;
-        // the last stage holds Q and dO until they are in TMEM
-        if (j == C::QDO_STAGE && !mbar_wait(&bar[C::B_IN], 0, wc)) break;
-        uint64_t* f = &bar[C::B_KVF + s];
-        mbar_arrive_expect_tx(f, 2 * C::TILE);
-#pragma unroll
-        for (int c = 0; c < C::KCH; ++c) {
-          tma_load_3d(smem + C::OFF_K + s * C::TILE + c * C::CHUNK, &tmK, f, c * 64, j * C::BN, bh);
-          tma_load_3d(smem + C::OFF_V + s * C::TILE + c * C::CHUNK, &tmV, f, c * 64, j * C::BN, bh);
-        }
-        issued = j + 1;
-      }
-      drain_wait(&bar[C::B_QDO], 0);
-      for (int j = max(0, issued - C::STAGES); j < issued; ++j)
-        drain_wait(&bar[C::B_KVF + j % C::STAGES], (j / C::STAGES) & 1);
+      for (int r = max(0, ru - C::STAGES); r < ru; ++r)
+        drain_wait(&bar[C::B_KVF + r % C::STAGES], (r / C::STAGES) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // Halves of each key block (64 keys, one per compute group) interleaved:
-    //   S_0 dP_0 S_1 dP_1 | dQ_0 S_0' dP_0' dQ_1 S_1' dP_1' | ...  (' = next block)
-    if (nkb > 0) {
-      constexpr uint32_t kIdescS = idesc_bf16_f32(128, 64, false, false);
-      constexpr uint32_t kIdescQ = idesc_bf16_f32(128, D, false, true);
+    constexpr uint32_t kIdescS = idesc_bf16_f32(128, 64, false, false);
+    constexpr uint32_t kIdescQ = idesc_bf16_f32(128, D, false, true);
+    int ru = 0, gb = 0, at = 0;
+    bool ok = true;
+    for (int t = 0; ok && t < count; ++t) {
+      int bh, q0, nkb;
+      block(t, bh, q0, nkb);
+      if (nkb == 0) continue;
+      const int rb = ru + 1;  // ring use of key block 0
       // S_h = Q K_h^T and dP_h = dO V_h^T for half h of key block j (N = 64). The
       // S_h columns still hold dS_h of block j-1, read by dQ of block j-1 that
       // this thread issued earlier (in-order execution); group h signalled dS_h
       // of block j-1 only after reading S_h and dP_h of it.
       auto scores = [&](int j, int h) {
-        const int s = j % C::STAGES;
+        const int s = (rb + j) % C::STAGES;
         const uint64_t k_k =
             sdesc_sw128(smem_u32(smem + C::OFF_K + s * C::TILE + h * C::HALF_ROWS), 16, 1024);
         const uint64_t v_k =
@@ -650,17 +715,23 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tmQ, const CUtensorMap
         }
         umma_commit_w(&bar[C::B_DPF + h]);
       };
-      bool ok = warp_wait(&bar[C::B_IN], 0, wc) && warp_wait(&bar[C::B_KVF], 0, wc);
-      if (ok) {
-        tc_fence_after();
-        scores(0, 0);
-        scores(0, 1);
-      }
+      // Q and dO are in TMEM (their slot may be refilled); key block 0 landed
+      if (!warp_wait(&bar[C::B_IN], at & 1, wc)) break;
+      if (lane == 0) mbar_arrive(&bar[C::B_KVE + ru % C::STAGES]);
+      if (!warp_wait(&bar[C::B_KVF + rb % C::STAGES], (rb / C::STAGES) & 1, wc)) break;
+      tc_fence_after();
+      scores(0, 0);
+      scores(0, 1);
       for (int j = 0; ok && j < nkb; ++j) {
-        const int s = j % C::STAGES;
+        const int s = (rb + j) % C::STAGES;
         for (int h = 0; ok && h < 2; ++h) {
           // dQ += dS_h K_h
-          if (!warp_wait(&bar[C::B_DSF + h], j & 1, wc)) { ok = false; break; }
+          if (!warp_wait(&bar[C::B_DSF + h], (gb + j) & 1, wc)) { ok = false; break; }
+          // the previous query block's dQ has been read out of TMEM
+          if (j == 0 && h == 0 && at >= 1 && !warp_wait(&bar[C::B_EPI], (at - 1) & 1, wc)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           const uint64_t k_mn = sdesc_sw128(
               smem_u32(smem + C::OFF_K + s * C::TILE + h * C::HALF_ROWS), C::CHUNK, 1024);
@@ -670,8 +741,8 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tmQ, const CUtensorMap
                       sdesc_add(k_mn, kk * 2048), kIdescQ, (j > 0 || h > 0 || kk > 0) ? 1u : 0u);
           if (h == 1) umma_commit_w(&bar[C::B_KVE + s]);  // last reader of K_j, V_j
           if (j + 1 < nkb) {
-            if (h == 0 &&
-                !warp_wait(&bar[C::B_KVF + (j + 1) % C::STAGES], ((j + 1) / C::STAGES) & 1, wc)) {
+            if (h == 0 && !warp_wait(&bar[C::B_KVF + (rb + j + 1) % C::STAGES],
+                                     ((rb + j + 1) / C::STAGES) & 1, wc)) {
               ok = false;
               break;
             }
@@ -680,120 +751,111 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tmQ, const CUtensorMap
           }
         }
       }
+      if (!ok) break;
       umma_commit_w(&bar[C::B_ACC]);
-      umma_commit_w(&bar[C::B_DRAIN]);
-      drain_wait(&bar[C::B_DRAIN], 0);
+      ru += 1 + nkb;
+      gb += nkb;
+      ++at;
     }
+    umma_commit_w(&bar[C::B_DRAIN]);
+    drain_wait(&bar[C::B_DRAIN], 0);
   } else if (warp >= 4) {
     // ------------------------------------------------------------ P, dS
     const int h = (warp - 4) >> 2;            // which half of the key columns
     const int r = (warp & 3) * 32 + lane;     // query row = TMEM lane
-    const int q = q0 + r;
     const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    const bool row_ok = q < p.n;
-    const size_t ws_row = (size_t)bh * p.n_pad + q;  // q < n_pad always
-    const float nl2 = p.nL2[ws_row];
-    const float nd = p.nD[ws_row];
     const float sl2 = p.scale_log2;
-    bool ok = nkb == 0 || warp_wait(&bar[C::B_QDO], 0, wc);
-    if (ok && nkb > 0) {
-      // Group 0 moves row r of Q into TMEM, group 1 row r of dO: the row's 16-byte
-      // pieces in the 128-byte-swizzled tile (piece j of a chunk row at j ^ (r % 8)).
-      const uint8_t* tile = smem + (h == 0 ? C::OFF_K : C::OFF_V) + C::QDO_STAGE * C::TILE;
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        uint32_t v[32];
-        const uint8_t* row = tile + c * C::CHUNK + r * 128;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint4 x = *reinterpret_cast<const uint4*>(row + ((j ^ (r & 7)) << 4));
-          v[4 * j] = x.x;
-          v[4 * j + 1] = x.y;
-          v[4 * j + 2] = x.z;
-          v[4 * j + 3] = x.w;
-        }
-        tmem_st32(tl + (h == 0 ? C::COL_Q : C::COL_DO) + 32 * c, v);
-      }
-      tmem_st_wait();
+    int ru = 0, gb = 0, at = 0;
+    int prev_q = 0, prev_bh = 0;
+    bool ok = true;
+    // dQ row of block a (head pbh, query pq): group h writes columns [h D/2, (h+1) D/2)
+    auto epilogue = [&](int a, int pbh, int pq) {
+      if (!warp_wait(&bar[C::B_ACC], a & 1, wc)) return false;
+      tc_fence_after();
+      tmem_row_out<D, D / 2>(tl + C::COL_DQ + h * (D / 2), p.scale,
+                             p.dQ + ((size_t)pbh * p.n + pq) * D + h * (D / 2), pq < p.n);
       tc_fence_before();
-    }
-    mbar_arrive(&bar[C::B_IN]);
-    for (int j = 0; j < nkb; ++j) {
-      if (!warp_wait(&bar[C::B_SF + h], j & 1, wc)) { ok = false; break; }
-      tc_fence_after();
-      const int k0 = j * C::BN + 64 * h;  // key of this group's column 0
-      // Columns c >= vis are masked: past m, or key k0 + c > q under causal masking.
-      int vis = p.m - k0;
-      if (p.causal) vis = min(vis, q - k0 + 1);
-      const bool masked = __any_sync(0xffffffffu, vis < 64);
-      uint32_t sr[64];
-      tmem_ld32(tl + C::COL_S + 64 * h, sr);
-      tmem_ld32(tl + C::COL_S + 64 * h + 32, sr + 32);
-      tmem_ld_wait();
-      reg_fence32(sr);
-      reg_fence32(sr + 32);
-      probabilities64<false>(sr, nullptr, sl2, nullptr, nl2, 0, false);
-      if (masked) {
+      mbar_arrive(&bar[C::B_EPI]);
+      return true;
+    };
+    for (int t = 0; ok && t < count; ++t) {
+      int bh, q0, nkb;
+      block(t, bh, q0, nkb);
+      const int q = q0 + r;
+      if (nkb == 0) {  // no key visible (not reached for m >= 1): dQ = 0
+        if (q < p.n) {
+          const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (c >= vis) sr[c] = 0u;
+          for (int c = 0; c < D / 16; ++c)
+            reinterpret_cast<uint4*>(p.dQ + ((size_t)bh * p.n + q) * D + h * (D / 2))[c] = z;
+        }
+        continue;
       }
-      if (!warp_wait(&bar[C::B_DPF + h], j & 1, wc)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t w[32];
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t dr[32];
-        tmem_ld32(tl + C::COL_DP + 64 * h + 32 * half, dr);
+      const size_t ws_row = (size_t)bh * p.n_pad + q;  // q < n_pad always
+      const float nl2 = p.nL2[ws_row];
+      const float nd = p.nD[ws_row];
+      // Group 0 moves row r of Q into TMEM, group 1 row r of dO. The previous
+      // block's S and dP products, the only readers of these columns, are complete.
+      {
+        const int s = ru % C::STAGES;
+        if (!warp_wait(&bar[C::B_KVF + s], (ru / C::STAGES) & 1, wc)) { ok = false; break; }
+        tile_row_to_tmem<D>(smem + (h == 0 ? C::OFF_K : C::OFF_V) + s * C::TILE, r,
+                            tl + (h == 0 ? C::COL_Q : C::COL_DO));
+        tc_fence_before();
+      }
+      mbar_arrive(&bar[C::B_IN]);
+      // The previous block's dQ leaves TMEM while this block's first products run.
+      if (at >= 1 && !epilogue(at - 1, prev_bh, prev_q)) { ok = false; break; }
+      for (int j = 0; j < nkb; ++j) {
+        if (!warp_wait(&bar[C::B_SF + h], (gb + j) & 1, wc)) { ok = false; break; }
+        tc_fence_after();
+        const int k0 = j * C::BN + 64 * h;  // key of this group's column 0
+        // Columns c >= vis are masked: past m, or key k0 + c > q under causal masking.
+        int vis = p.m - k0;
+        if (p.causal) vis = min(vis, q - k0 + 1);
+        const bool masked = __any_sync(0xffffffffu, vis < 64);
+        uint32_t sr[64];
+        tmem_ld32(tl + C::COL_S + 64 * h, sr);
+        tmem_ld32(tl + C::COL_S + 64 * h + 32, sr + 32);
         tmem_ld_wait();
-        reg_fence32(dr);
-        dscores32<false>(sr + 32 * half, dr, w + 16 * half, nullptr, nd);
-      }
-      // dS (bf16) over this group's first 32 S columns, already read.
-      tmem_st32(tl + C::COL_S + 64 * h, w);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&bar[C::B_DSF + h]);
-    }
-
-    // ------------------------------------------------------------ dQ out
-    // Group h writes columns [h D/2, (h + 1) D/2) of its row.
-    if (ok && (nkb == 0 || warp_wait(&bar[C::B_ACC], 0, wc))) {
-      tc_fence_after();
-      __nv_bfloat16* dst_row = p.dQ + ((size_t)bh * p.n + q) * D + h * (D / 2);
+        reg_fence32(sr);
+        reg_fence32(sr + 32);
+        probabilities64<false>(sr, nullptr, sl2, nullptr, nl2, 0, false);
+        if (masked) {
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        uint32_t o[32];
-        if (nkb > 0) {
-          tmem_ld32(tl + C::COL_DQ + h * (D / 2) + 32 * c, o);
+          for (int c = 0; c < 64; ++c)
+            if (c >= vis) sr[c] = 0u;
+        }
+        if (!warp_wait(&bar[C::B_DPF + h], (gb + j) & 1, wc)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t w[32];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t dr[32];
+          tmem_ld32(tl + C::COL_DP + 64 * h + 32 * half, dr);
           tmem_ld_wait();
-          reg_fence32(o);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = 0u;
+          reg_fence32(dr);
+          dscores32<false>(sr + 32 * half, dr, w + 16 * half, nullptr, nd);
         }
-        uint32_t w[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-          w[e] = pack_bf16(__uint_as_float(o[2 * e]) * p.scale,
-                           __uint_as_float(o[2 * e + 1]) * p.scale);
-        if (row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(dst_row + 32 * c);
-          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-          dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
-          dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
-        }
+        // dS (bf16) over this group's first 32 S columns, already read.
+        tmem_st32(tl + C::COL_S + 64 * h, w);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bar[C::B_DSF + h]);
       }
+      prev_q = q;
+      prev_bh = bh;
+      ru += 1 + nkb;
+      gb += nkb;
+      ++at;
     }
+    if (ok && at >= 1) epilogue(at - 1, prev_bh, prev_q);
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, C::TMEM_COLS);
-  }
+  if (threadIdx.x == 0)
+    for (int b = 0; b < C::NBAR; ++b) mbar_inval(&bar[b]);
 }
 
 // ================================================================== preprocess
@@ -837,19 +899,49 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const __nv_bfloat16* __
   }
 }
 
-// The dK, dV and dQ passes in one launch: n_kv CTAs of the first, then n_dq of
-// the second, whose heavy blocks fill the SMs the first pass's tail leaves idle.
+// The gradient kernel: one CTA per SM (persistent). The list [n_kv key blocks,
+// then n_dq query blocks] is dealt out in rounds of P = grid size items, CTA c
+// taking item snake_item(r, c, P) of round r, so that it runs its share of the
+// dK/dV pass and then of the dQ pass; the lists are in launch order (heaviest
+// blocks first within a group of heads).
 template <int D>
 __global__ void __launch_bounds__(384, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                const __grid_constant__ CUtensorMap tmNL2, const __grid_constant__ CUtensorMap tmND,
                const KvParams kp, const DqParams qp, int n_kv, int n_dq) {
-  const int b = blockIdx.x;
-  if (b < n_kv)
-    dkdv_cta<D>(tmQ, tmK, tmV, tmdO, tmNL2, tmND, kp, b);
-  else
-    dq_cta<D>(tmQ, tmK, tmV, tmdO, qp, b - n_kv);
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint32_t tmem_slot;
+  __shared__ uint32_t abort_word;
+  uint8_t* smem = align1024(smem_raw);
+  const WaitCtx wc{&abort_word, &g_bwd_status};
+  if (threadIdx.x == 0) abort_word = 0u;
+  if ((threadIdx.x >> 5) == 1) {
+    tmem_alloc(&tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  const int P = gridDim.x, c = blockIdx.x;
+  const int total = n_kv + n_dq;
+  // Items grow with the round: this CTA's key blocks come first, then query blocks.
+  int kv_rounds = 0;
+  while (snake_item(kv_rounds, c, P) < n_kv) ++kv_rounds;
+  int rounds = kv_rounds;
+  while (snake_item(rounds, c, P) < total) ++rounds;
+  if (kv_rounds > 0) dkdv_run<D>(tmQ, tmK, tmV, tmdO, tmNL2, tmND, kp, smem, tmem, 0, c, P, kv_rounds, wc);
+  if (rounds > kv_rounds)
+    dq_run<D>(tmQ, tmK, tmV, tmdO, qp, smem, tmem, kv_rounds, c, P, n_kv, rounds - kv_rounds, wc);
+
+  tc_fence_before();
+  __syncthreads();
+  if ((threadIdx.x >> 5) == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
 }
 
 template <int D>
@@ -857,13 +949,15 @@ cudaError_t launch_bwd_d(const BwdArgs& a, bool with_kv, bool with_dq, cudaStrea
   using KC = KvCfg<D>;
   using QC = QCfg<D>;
   static_assert(KC::BQ == QC::BM && KC::BN == QC::BN, "the passes share the tensor maps");
+  static_assert(KC::THREADS == QC::THREADS, "the passes share the launch");
   CUtensorMap mq, mk, mv, mdo, ml2, md;
-  if (make_bf16_head_map(&mq, a.Q, a.BH, a.n, D, KC::BQ) != CUDA_SUCCESS ||
+  // Q and dO, -L2 and -D travel in 64-row pieces; K and V in 128-row tiles.
+  if (make_bf16_head_map(&mq, a.Q, a.BH, a.n, D, 64) != CUDA_SUCCESS ||
       make_bf16_head_map(&mk, a.K, a.BH, a.m, D, KC::BN) != CUDA_SUCCESS ||
       make_bf16_head_map(&mv, a.V, a.BH, a.m, D, KC::BN) != CUDA_SUCCESS ||
-      make_bf16_head_map(&mdo, a.dO, a.BH, a.n, D, KC::BQ) != CUDA_SUCCESS ||
-      make_f32_row_map(&ml2, a.ws_nL2, a.BH, a.n_pad, KC::BQ) != CUDA_SUCCESS ||
-      make_f32_row_map(&md, a.ws_nD, a.BH, a.n_pad, KC::BQ) != CUDA_SUCCESS)
+      make_bf16_head_map(&mdo, a.dO, a.BH, a.n, D, 64) != CUDA_SUCCESS ||
+      make_f32_row_map(&ml2, a.ws_nL2, a.BH, a.n_pad, 64) != CUDA_SUCCESS ||
+      make_f32_row_map(&md, a.ws_nD, a.BH, a.n_pad, 64) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   KvParams kp;
   kp.dK = static_cast<__nv_bfloat16*>(a.dK);
@@ -896,8 +990,12 @@ cudaError_t launch_bwd_d(const BwdArgs& a, bool with_kv, bool with_dq, cudaStrea
   cudaError_t e =
       cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  bwd_kernel<D><<<(unsigned)(n_kv + n_dq), KC::THREADS, smem, stream>>>(mq, mk, mv, mdo, ml2, md,
-                                                                        kp, qp, n_kv, n_dq);
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int grid = n_kv + n_dq < sms ? n_kv + n_dq : sms;
+  bwd_kernel<D><<<(unsigned)grid, KC::THREADS, smem, stream>>>(mq, mk, mv, mdo, ml2, md, kp, qp,
+                                                               n_kv, n_dq);
   return cudaGetLastError();
 }
 
