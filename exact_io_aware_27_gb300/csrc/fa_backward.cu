@@ -899,11 +899,11 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const __nv_bfloat16* __
   }
 }
 
-// The gradient kernel: one CTA per SM (persistent). The list [n_kv key blocks,
-// then n_dq query blocks] is dealt out in rounds of P = grid size items, CTA c
-// taking item snake_item(r, c, P) of round r, so that it runs its share of the
-// dK/dV pass and then of the dQ pass; the lists are in launch order (heaviest
-// blocks first within a group of heads).
+// The gradient kernel: one CTA per SM (persistent). The n_kv key blocks and then
+// the n_dq query blocks are dealt out in rounds of P = grid size items (CTA c takes
+// snake_item(r, c, P) of round r), so that each CTA runs its share of the dK/dV
+// pass and then of the dQ pass; the lists are in launch order (heaviest blocks
+// first within a group of heads).
 template <int D>
 __global__ void __launch_bounds__(384, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -926,15 +926,13 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = tmem_slot;
 
   const int P = gridDim.x, c = blockIdx.x;
-  const int total = n_kv + n_dq;
-  // Items grow with the round: this CTA's key blocks come first, then query blocks.
-  int kv_rounds = 0;
+  // Each list is dealt separately; the query blocks in reverse CTA order, so that
+  // the CTAs left with one key block more get no query block more.
+  int kv_rounds = 0, dq_rounds = 0;
   while (snake_item(kv_rounds, c, P) < n_kv) ++kv_rounds;
-  int rounds = kv_rounds;
-  while (snake_item(rounds, c, P) < total) ++rounds;
+  while (snake_item(dq_rounds, P - 1 - c, P) < n_dq) ++dq_rounds;
   if (kv_rounds > 0) dkdv_run<D>(tmQ, tmK, tmV, tmdO, tmNL2, tmND, kp, smem, tmem, 0, c, P, kv_rounds, wc);
-  if (rounds > kv_rounds)
-    dq_run<D>(tmQ, tmK, tmV, tmdO, qp, smem, tmem, kv_rounds, c, P, n_kv, rounds - kv_rounds, wc);
+  if (dq_rounds > 0) dq_run<D>(tmQ, tmK, tmV, tmdO, qp, smem, tmem, 0, P - 1 - c, P, 0, dq_rounds, wc);
 
   tc_fence_before();
   __syncthreads();
