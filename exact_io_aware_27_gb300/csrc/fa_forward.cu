@@ -14,20 +14,23 @@
 // no rescaling of O.
 //
 // GB300 mapping (one CTA per (pair of query tiles, head), 384 threads):
-//   warp 0       TMA producer: Q of both tiles once, then K_j and V_j into a
-//                STAGES-deep ring shared by the two tiles
-//   warp 1       MMA issuer (whole warp, one elected lane issues):
-//                S0 = Q0 K_j^T, S1 = Q1 K_j^T, then O0 += P0 V_j, O1 += P1 V_j
-//                (P read from TMEM); S_t of block j+1 waits for O_t += P_t V_j
+//   warp 0       TMA producer: both Q tiles (the ring's first slot), then K_j
+//                and V_j (128 keys each) into a ring shared by the two tiles
+//   warp 1       MMA issuer (whole warp, one elected lane issues). Keys are
+//                taken in steps of 64 (half a loaded block): S_t = Q_t K^T (TS:
+//                Q_t read from TMEM) and O_t += P_t V (TS: P_t read from TMEM),
+//                the two tiles alternating; S_t of step k+1 is issued right
+//                after O_t += P_t V of step k, over the same columns
 //   warps 4..7   softmax of tile 0, warps 8..11 softmax of tile 1: thread r
-//                owns query row r of its tile (= TMEM lane r); reads the S row
-//                with tcgen05.ld, masks, updates (m, l) in base 2 (exp2 via
-//                ex2.approx), writes P as bf16 over the first 64 columns of
-//                its own S row, rescales its O row when m moved, and runs the
-//                epilogue. While one tile's softmax runs, the tensor cores work
-//                on the other tile.
-// TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256, 256+d) O1 [256+d, 256+2d).
-// Scores, probabilities and the accumulators never leave the SM.
+//                first moves row r of Q_t into TMEM, then owns query row r of its
+//                tile (= TMEM lane r): reads the 64 S columns of a step with
+//                tcgen05.ld, masks, updates (m, l) in base 2 (exp2 via
+//                ex2.approx), writes P as bf16 over the first 32 of them,
+//                rescales its O row when m moved, and runs the epilogue. While
+//                one tile's softmax runs, the tensor cores work on the other.
+// TMEM (512 columns at d = 128): Q0, Q1 (d/2 each, bf16 pairs), S0, S1 (64
+// each), O0, O1 (d each). Scores, probabilities and the accumulators never
+// leave the SM.
 #include "fa_internal.h"
 #include "sm103.cuh"
 
@@ -44,29 +47,31 @@ template <int D>
 struct FwdCfg {
   static constexpr int BM = 128;                 // query rows per tile = TMEM lanes
   static constexpr int TILES = 2;                // query tiles per CTA
-  static constexpr int BN = 128;                 // keys per block
+  static constexpr int BN = 128;                 // keys per loaded block (two halves of 64)
   static constexpr int KCH = D / 64;             // 128-byte column chunks per row
   static constexpr int CHUNK = 128 * 128;        // bytes of one chunk of a 128-row tile
   static constexpr int TILE = KCH * CHUNK;       // bytes of a Q, K or V tile
-  static constexpr int STAGES = (D == 128) ? 2 : 4;
-  static constexpr int OFF_Q = 0;                // TILES query tiles
-  static constexpr int OFF_K = OFF_Q + TILES * TILE;
-  static constexpr int OFF_V = OFF_K + STAGES * TILE;
-  static constexpr int OFF_BAR = OFF_V + STAGES * TILE;
+  static constexpr int HALF_ROWS = 64 * 128;     // bytes of 64 rows of one chunk
+  // Ring of K/V blocks; its first use holds the two Q tiles until they are in TMEM.
+  static constexpr int STAGES = (D == 128) ? 3 : 6;
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = STAGES * TILE;
+  static constexpr int OFF_BAR = 2 * STAGES * TILE;
   // barrier slots
-  static constexpr int B_Q = 0;
-  static constexpr int B_KF = 1;
-  static constexpr int B_KE = B_KF + STAGES;
-  static constexpr int B_VF = B_KE + STAGES;
-  static constexpr int B_VE = B_VF + STAGES;
-  static constexpr int B_SF = B_VE + STAGES;    // + tile: S_t ready
-  static constexpr int B_PF = B_SF + TILES;     // + 2 tile + half: half of P_t written
-  static constexpr int B_PVD = B_PF + 2 * TILES;  // + tile: O_t += P_t V done
+  static constexpr int B_KVF = 0;                // + slot: the slot's copies landed
+  static constexpr int B_KVE = STAGES;           // + slot: the slot may be refilled
+  static constexpr int B_IN = 2 * STAGES;        // Q tiles in TMEM (256 arrivals)
+  static constexpr int B_SF = B_IN + 1;          // + tile: S_t of the current step done
+  static constexpr int B_PF = B_SF + TILES;      // + tile: P_t written (128 arrivals)
+  static constexpr int B_PVD = B_PF + TILES;     // + tile: the tile's last O += P V done
   static constexpr int B_DRAIN = B_PVD + TILES;
   static constexpr int NBAR = B_DRAIN + 1;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;
-  static constexpr uint32_t COL_S = 0;           // + 128 * tile
-  static constexpr uint32_t COL_O = 256;         // + D * tile
+  // TMEM columns: Q_t as bf16 pairs (the A operand of S_t = Q_t K^T), S_t of one
+  // 64-key step (then P_t as bf16 pairs over its first 32 columns), O_t.
+  static constexpr uint32_t COL_Q = 0;           // + (D / 2) * tile
+  static constexpr uint32_t COL_S = D;           // + 64 * tile
+  static constexpr uint32_t COL_O = D + 128;     // + D * tile
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr int THREADS = 384;
   static_assert(COL_O + TILES * D <= TMEM_COLS, "TMEM budget");
@@ -89,12 +94,12 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
-// Key blocks a tile of rows [q0, q0 + 128) visits (0 if the tile is past n).
-__device__ __forceinline__ int tile_blocks(int q0, int n, int m, int causal) {
+// 64-key steps a tile of rows [q0, q0 + 128) visits (0 if the tile is past n).
+__device__ __forceinline__ int tile_steps(int q0, int n, int m, int causal) {
   if (q0 >= n) return 0;
-  int nkb = (m + 127) / 128;
-  if (causal) nkb = min(nkb, (min(q0 + 127, n - 1)) / 128 + 1);  // keys k <= q
-  return nkb;
+  int nh = (m + 63) / 64;
+  if (causal) nh = min(nh, (min(q0 + 127, n - 1)) / 64 + 1);  // keys k <= q
+  return nh;
 }
 
 template <int D>
@@ -117,22 +122,20 @@ __global__ void __launch_bounds__(384, 1)
   grouped_tile(blockIdx.x, p.BH, p.num_pairs, p.group, pair, bh);
   if (p.causal) pair = p.num_pairs - 1 - pair;
   const int qs = pair * (C::TILES * C::BM);
-  const int nkb0 = tile_blocks(qs, p.n, p.m, p.causal);
-  const int nkb1 = tile_blocks(qs + C::BM, p.n, p.m, p.causal);
-  const int nkb = max(nkb0, nkb1);
+  const int nh0 = tile_steps(qs, p.n, p.m, p.causal);
+  const int nh1 = tile_steps(qs + C::BM, p.n, p.m, p.causal);
+  const int nh = max(nh0, nh1);     // 64-key steps of the CTA
+  const int nkb = (nh + 1) / 2;     // 128-key blocks loaded
 
   if (threadIdx.x == 0) {
-    mbar_init(&bar[C::B_Q], 1);
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&bar[C::B_KF + s], 1);
-      mbar_init(&bar[C::B_KE + s], 1);
-      mbar_init(&bar[C::B_VF + s], 1);
-      mbar_init(&bar[C::B_VE + s], 1);
+      mbar_init(&bar[C::B_KVF + s], 1);
+      mbar_init(&bar[C::B_KVE + s], 1);
     }
+    mbar_init(&bar[C::B_IN], 256);
     for (int t = 0; t < C::TILES; ++t) {
       mbar_init(&bar[C::B_SF + t], 1);
-      mbar_init(&bar[C::B_PF + 2 * t], 128);
-      mbar_init(&bar[C::B_PF + 2 * t + 1], 128);
+      mbar_init(&bar[C::B_PF + t], 128);
       mbar_init(&bar[C::B_PVD + t], 1);
     }
     mbar_init(&bar[C::B_DRAIN], 1);
@@ -150,186 +153,192 @@ __global__ void __launch_bounds__(384, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    // Ring use 0: the two Q tiles (slot 0's K and V buffers); use j + 1: K_j, V_j.
+    if (lane == 0 && nh > 0) {
       tma_prefetch_map(&tmQ);
       tma_prefetch_map(&tmK);
       tma_prefetch_map(&tmV);
-      mbar_arrive_expect_tx(&bar[C::B_Q], C::TILES * C::TILE);
+      int issued = 0;
+      for (int u = 0; u <= nkb; ++u) {
+        const int s = u % C::STAGES;
+        if (u >= C::STAGES && !mbar_wait(&bar[C::B_KVE + s], ((u / C::STAGES) & 1) ^ 1, wc))
+          break;
+        uint64_t* f = &bar[C::B_KVF + s];
+        mbar_arrive_expect_tx(f, 2 * C::TILE);
 #pragma unroll
-      for (int t = 0; t < C::TILES; ++t)
-#pragma unroll
-        for (int c = 0; c < C::KCH; ++c)
-          tma_load_3d(smem + C::OFF_Q + t * C::TILE + c * C::CHUNK, &tmQ, &bar[C::B_Q], c * 64,
-                      qs + t * C::BM, bh);
-      int nk = 0, nv = 0;  // loads issued
-      for (int j = 0; j < nkb; ++j) {
-        const int s = j % C::STAGES;
-        const uint32_t ph = (j / C::STAGES) & 1;
-        if (j >= C::STAGES && !mbar_wait(&bar[C::B_KE + s], ph ^ 1, wc)) break;
-        mbar_arrive_expect_tx(&bar[C::B_KF + s], C::TILE);
-#pragma unroll
-        for (int c = 0; c < C::KCH; ++c)
-          tma_load_3d(smem + C::OFF_K + s * C::TILE + c * C::CHUNK, &tmK, &bar[C::B_KF + s],
-                      c * 64, j * C::BN, bh);
-        nk = j + 1;
-        if (j >= C::STAGES && !mbar_wait(&bar[C::B_VE + s], ph ^ 1, wc)) break;
-        mbar_arrive_expect_tx(&bar[C::B_VF + s], C::TILE);
-#pragma unroll
-        for (int c = 0; c < C::KCH; ++c)
-          tma_load_3d(smem + C::OFF_V + s * C::TILE + c * C::CHUNK, &tmV, &bar[C::B_VF + s],
-                      c * 64, j * C::BN, bh);
-        nv = j + 1;
+        for (int c = 0; c < C::KCH; ++c) {
+          if (u == 0) {
+            tma_load_3d(smem + C::OFF_K + c * C::CHUNK, &tmQ, f, c * 64, qs, bh);
+            tma_load_3d(smem + C::OFF_V + c * C::CHUNK, &tmQ, f, c * 64, qs + C::BM, bh);
+          } else {
+            tma_load_3d(smem + C::OFF_K + s * C::TILE + c * C::CHUNK, &tmK, f, c * 64,
+                        (u - 1) * C::BN, bh);
+            tma_load_3d(smem + C::OFF_V + s * C::TILE + c * C::CHUNK, &tmV, f, c * 64,
+                        (u - 1) * C::BN, bh);
+          }
+        }
+        issued = u + 1;
       }
       // Let every copy this thread issued land before the CTA can exit.
-      drain_wait(&bar[C::B_Q], 0);
-      for (int j = max(0, nk - C::STAGES); j < nk; ++j)
-        drain_wait(&bar[C::B_KF + j % C::STAGES], (j / C::STAGES) & 1);
-      for (int j = max(0, nv - C::STAGES); j < nv; ++j)
-        drain_wait(&bar[C::B_VF + j % C::STAGES], (j / C::STAGES) & 1);
+      for (int u = max(0, issued - C::STAGES); u < issued; ++u)
+        drain_wait(&bar[C::B_KVF + u % C::STAGES], (u / C::STAGES) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // The whole warp runs the loop (operands stay warp-uniform); elect.sync picks
-    // the issuing lane. Descriptors are built once per buffer and advanced by
-    // compile-time byte offsets.
-    constexpr uint32_t kIdescS = idesc_bf16_f32(128, C::BN, false, false);
-    constexpr uint32_t kIdescO = idesc_bf16_f32(128, D, false, true);
-    bool ok = warp_wait(&bar[C::B_Q], 0, wc);
-    for (int j = 0; ok && j < nkb; ++j) {
-      const int s = j % C::STAGES;
-      const uint32_t ph = (j / C::STAGES) & 1;
-      if (!warp_wait(&bar[C::B_KF + s], ph, wc)) break;
-      const uint64_t dK_k = sdesc_sw128(smem_u32(smem + C::OFF_K + s * C::TILE), 16, 1024);
-#pragma unroll
-      for (int t = 0; t < C::TILES; ++t) {
-        if (j >= (t == 0 ? nkb0 : nkb1)) continue;
-        // S_t's columns hold P_t of block j-1 until O_t += P_t V_{j-1} is done.
-        if (j >= 1 && !warp_wait(&bar[C::B_PVD + t], (j - 1) & 1, wc)) { ok = false; break; }
-        tc_fence_after();
-        const uint64_t dQ_k = sdesc_sw128(smem_u32(smem + C::OFF_Q + t * C::TILE), 16, 1024);
+    // Keys in steps of 64 (half a loaded block); the two tiles alternate:
+    //   S_0(0) S_1(0) | O_0 += P_0(0) V, S_0(1), O_1 += P_1(0) V, S_1(1) | ...
+    // S_t(k+1) overwrites P_t(k), read by the O_t product issued just before it
+    // (tcgen05.mma instructions of one thread execute in order).
+    if (nh > 0) {
+      constexpr uint32_t kIdescS = idesc_bf16_f32(128, 64, false, false);
+      constexpr uint32_t kIdescO = idesc_bf16_f32(128, D, false, true);
+      auto slot_of = [&](int k) { return ((k >> 1) + 1) % C::STAGES; };
+      auto scores = [&](int t, int k) {
+        const uint64_t b_k = sdesc_sw128(
+            smem_u32(smem + C::OFF_K + slot_of(k) * C::TILE + (k & 1) * C::HALF_ROWS), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
-          umma_ss_w(tmem + C::COL_S + 128 * t, sdesc_add(dQ_k, off), sdesc_add(dK_k, off),
-                    kIdescS, kk > 0);
+          umma_ts_w(tmem + C::COL_S + 64 * t, tmem + C::COL_Q + (D / 2) * t + kk * 8,
+                    sdesc_add(b_k, off), kIdescS, kk > 0);
         }
         umma_commit_w(&bar[C::B_SF + t]);
+      };
+      auto pv = [&](int t, int k) {
+        const uint64_t b_mn = sdesc_sw128(
+            smem_u32(smem + C::OFF_V + slot_of(k) * C::TILE + (k & 1) * C::HALF_ROWS), C::CHUNK,
+            1024);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_ts_w(tmem + C::COL_O + D * t, tmem + C::COL_S + 64 * t + kk * 8,
+                    sdesc_add(b_mn, kk * 2048), kIdescO, (k > 0 || kk > 0) ? 1u : 0u);
+      };
+      const int nht[2] = {nh0, nh1};
+      bool ok = warp_wait(&bar[C::B_IN], 0, wc);
+      if (ok) {
+        if (lane == 0) mbar_arrive(&bar[C::B_KVE + 0]);  // the Q tiles are in TMEM
+        ok = warp_wait(&bar[C::B_KVF + 1 % C::STAGES], (1 / C::STAGES) & 1, wc);
       }
-      if (!ok) break;
-      umma_commit_w(&bar[C::B_KE + s]);
-      if (!warp_wait(&bar[C::B_VF + s], ph, wc)) break;
-      const uint64_t dV_mn = sdesc_sw128(smem_u32(smem + C::OFF_V + s * C::TILE), C::CHUNK, 1024);
-#pragma unroll
-      for (int t = 0; t < C::TILES; ++t) {
-        if (j >= (t == 0 ? nkb0 : nkb1)) continue;
-        const uint32_t aP = tmem + C::COL_S + 128 * t;  // P_t: first 64 columns of S_t
-        // Keys 0..63 as soon as their P is written, then keys 64..127.
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          if (!warp_wait(&bar[C::B_PF + 2 * t + h], j & 1, wc)) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
-            umma_ts_w(tmem + C::COL_O + D * t, aP + kk * 8, sdesc_add(dV_mn, kk * 2048), kIdescO,
-                      (j > 0 || kk > 0) ? 1u : 0u);
+      if (ok) {
+        tc_fence_after();
+        if (nh0 > 0) scores(0, 0);
+        if (nh1 > 0) scores(1, 0);
+      }
+      for (int k = 0; ok && k < nh; ++k) {
+        if (k + 1 < nh && ((k + 1) & 1) == 0) {  // step k+1 opens block (k+1)/2
+          const int u = ((k + 1) >> 1) + 1;
+          if (!warp_wait(&bar[C::B_KVF + u % C::STAGES], (u / C::STAGES) & 1, wc)) break;
         }
-        if (!ok) break;
-        umma_commit_w(&bar[C::B_PVD + t]);
+#pragma unroll
+        for (int t = 0; t < C::TILES; ++t) {
+          if (k >= nht[t]) continue;
+          if (!warp_wait(&bar[C::B_PF + t], k & 1, wc)) { ok = false; break; }
+          tc_fence_after();
+          pv(t, k);
+          if (k + 1 < nht[t])
+            scores(t, k + 1);
+          else
+            umma_commit_w(&bar[C::B_PVD + t]);
+        }
+        // both tiles are done with block k/2 once its second step is issued
+        if (ok && ((k & 1) || k + 1 == nh)) umma_commit_w(&bar[C::B_KVE + slot_of(k)]);
       }
-      if (!ok) break;
-      umma_commit_w(&bar[C::B_VE + s]);
+      umma_commit_w(&bar[C::B_DRAIN]);
+      drain_wait(&bar[C::B_DRAIN], 0);
     }
-    umma_commit_w(&bar[C::B_DRAIN]);
-    drain_wait(&bar[C::B_DRAIN], 0);
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
     const int t = (warp - 4) >> 2;                 // query tile of this warpgroup
     const int row = ((warp - 4) & 3) * 32 + lane;  // row in the tile = TMEM lane
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    const uint32_t scol = lane_base + C::COL_S + 128 * t;
+    const uint32_t scol = lane_base + C::COL_S + 64 * t;
     const uint32_t ocol = lane_base + C::COL_O + D * t;
     const int qg = qs + t * C::BM + row;
-    const int nkb_t = t == 0 ? nkb0 : nkb1;
+    const int nh_t = t == 0 ? nh0 : nh1;
     const float sl2 = p.scale_log2;
     float m_ref = -INFINITY;  // reference maximum of S * scale * log2(e)
     float l_run = 0.f;        // sum of exp2(S * scale * log2(e) - m_ref)
-    bool ok = true;
-    for (int j = 0; j < nkb_t; ++j) {
-      if (!warp_wait(&bar[C::B_SF + t], j & 1, wc)) {
+    bool ok = nh == 0 || warp_wait(&bar[C::B_KVF], 0, wc);
+    if (ok && nh > 0) {
+      // Row `row` of Q_t into TMEM: the row's 16-byte pieces in the 128-byte-
+      // swizzled tile (piece j of a chunk row at j ^ (row % 8)).
+      const uint8_t* tile = smem + (t == 0 ? C::OFF_K : C::OFF_V);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t v[32];
+        const uint8_t* src = tile + c * C::CHUNK + row * 128;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint4 x = *reinterpret_cast<const uint4*>(src + ((j ^ (row & 7)) << 4));
+          v[4 * j] = x.x;
+          v[4 * j + 1] = x.y;
+          v[4 * j + 2] = x.z;
+          v[4 * j + 3] = x.w;
+        }
+        tmem_st32(lane_base + C::COL_Q + (D / 2) * t + 32 * c, v);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+    }
+    if (nh > 0) mbar_arrive(&bar[C::B_IN]);
+    for (int k = 0; ok && k < nh_t; ++k) {
+      if (!warp_wait(&bar[C::B_SF + t], k & 1, wc)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t sr[128];
-      tmem_ld32(scol + 0, sr);
+      uint32_t sr[64];
+      tmem_ld32(scol, sr);
       tmem_ld32(scol + 32, sr + 32);
-      tmem_ld32(scol + 64, sr + 64);
-      tmem_ld32(scol + 96, sr + 96);
       tmem_ld_wait();
       reg_fence32(sr);
       reg_fence32(sr + 32);
-      reg_fence32(sr + 64);
-      reg_fence32(sr + 96);
 
-      // Last visible column of this block for this row (ragged m, causal k <= q).
-      const int ks = j * C::BN;
+      // Last visible column of this step for this row (ragged m, causal k <= q).
+      const int ks = 64 * k;
       int lim = p.m - 1 - ks;
       if (p.causal) lim = min(lim, qg - ks);
-      if (lim < C::BN - 1) {
+      if (lim < 63) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
+        for (int c = 0; c < 64; ++c)
           if (c > lim) sr[c] = __float_as_uint(-INFINITY);
       }
       // Row maximum: eight chains of three-input maxima.
       float mx[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mx[k] = __uint_as_float(sr[k]);
+      for (int e = 0; e < 8; ++e) mx[e] = __uint_as_float(sr[e]);
 #pragma unroll
-      for (int c = 8; c < 128; c += 16)
+      for (int c = 8; c < 64; c += 16)
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mx[k] = max3f(mx[k], __uint_as_float(sr[c + k]), __uint_as_float(sr[c + 8 + k]));
+        for (int e = 0; e < 8; ++e)
+          mx[e] = max3f(mx[e], __uint_as_float(sr[c + e]), __uint_as_float(sr[c + 8 + e]));
       const float rmax = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]),
                                fmaxf(mx[6], mx[7])) * sl2;
       // Move the reference only when the row maximum passed it by the threshold.
       const bool move = rmax > m_ref + kRescaleThreshold;
       const float m_new = move ? rmax : m_ref;
-      const float corr = move ? ex2(m_ref - m_new) : 1.f;  // 0 on the first block
+      const float corr = move ? ex2(m_ref - m_new) : 1.f;  // 0 on the first step
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;  // no (-inf) - (-inf)
       m_ref = m_new;
-      // S_t(j) completing implies O_t += P_t V_{j-1} completed (issued before
-      // it), so the O row may be rescaled before this block's products start.
-      // When no row of the warp moved its reference (the common case) each half
-      // of P is signalled as soon as it is written; otherwise both halves are
-      // signalled after the rescale.
-      const bool rescale = j >= 1 && __any_sync(0xffffffffu, move);
-      // P = exp2(S * scale * log2(e) - m) in two halves of 64 keys, written as
-      // bf16 pairs over this row's own S columns.
+      // P = exp2(S * scale * log2(e) - m) as bf16 pairs over this row's own S
+      // columns.
       const uint64_t sl2x2 = f2pack(sl2, sl2);
       const uint64_t negm2 = f2pack(-m_use, -m_use);
       uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+      uint32_t pp[32];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pp[32];
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int e = 64 * h + 2 * c;
-          const uint64_t x2 =
-              ffma2(f2pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sl2x2, negm2);
-          float x0, x1;
-          f2unpack(x2, x0, x1);
-          const float p0 = ex2(x0), p1 = ex2(x1);
-          acc2[c & 3] = fadd2(acc2[c & 3], f2pack(p0, p1));
-          pp[c] = pack_bf16(p0, p1);
-        }
-        tmem_st32(scol + 32 * h, pp);
-        if (!rescale) {
-          tmem_st_wait();
-          tc_fence_before();
-          mbar_arrive(&bar[C::B_PF + 2 * t + h]);
-        }
+      for (int c = 0; c < 32; ++c) {
+        const uint64_t x2 = ffma2(
+            f2pack(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), sl2x2, negm2);
+        float x0, x1;
+        f2unpack(x2, x0, x1);
+        const float p0 = ex2(x0), p1 = ex2(x1);
+        acc2[c & 3] = fadd2(acc2[c & 3], f2pack(p0, p1));
+        pp[c] = pack_bf16(p0, p1);
       }
-      if (rescale) {
+      // S_t(k) completing implies O_t += P_t(k-1) V completed (issued before it),
+      // so the O row may be rescaled before this step's product is signalled.
+      if (k >= 1 && __any_sync(0xffffffffu, move)) {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
@@ -340,11 +349,11 @@ __global__ void __launch_bounds__(384, 1)
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
           tmem_st32(ocol + 32 * c, o);
         }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(&bar[C::B_PF + 2 * t]);
-        mbar_arrive(&bar[C::B_PF + 2 * t + 1]);
       }
+      tmem_st32(scol, pp);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bar[C::B_PF + t]);
       float s0, s1, s2, s3, s4, s5, s6, s7;
       f2unpack(acc2[0], s0, s1);
       f2unpack(acc2[1], s2, s3);
@@ -354,7 +363,7 @@ __global__ void __launch_bounds__(384, 1)
     }
 
     // ------------------------------------------------------------ epilogue
-    if (ok && nkb_t > 0 && warp_wait(&bar[C::B_PVD + t], (nkb_t - 1) & 1, wc)) {
+    if (ok && nh_t > 0 && warp_wait(&bar[C::B_PVD + t], 0, wc)) {
       tc_fence_after();
       const float inv_l = 1.f / l_run;
       __nv_bfloat16* orow = p.O + ((size_t)bh * p.n + qg) * D;
