@@ -405,6 +405,77 @@ def run_ours(args):
     return 0
 
 
+SOFTMAX_ROWS, SOFTMAX_COLS, SOFTMAX_SEED = 32768, 4096, 1100
+
+
+def run_online_softmax(args):
+    """The standalone online-softmax statistics kernel on rows shaped like the
+    benchmark's score rows (32768 rows of 4096 fp32, 512 MiB > L2): HBM bound."""
+    import exact_io_aware_27_gb300 as fa
+
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    x = wl.score_rows(SOFTMAX_ROWS, SOFTMAX_COLS, SOFTMAX_SEED + rank).to(dev)
+    m = torch.empty(SOFTMAX_ROWS, dtype=torch.float32, device=dev)
+    l = torch.empty_like(m)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(3, args.warmup)):
+        fa.fa_online_softmax_stats(x, m, l)
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(dev)
+    clocks.start()
+    time.sleep(0.2)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        fa.fa_online_softmax_stats(x, m, l)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    ms = max_over_ranks(e0.elapsed_time(e1), dev) / args.steps
+    nbytes = SOFTMAX_ROWS * SOFTMAX_COLS * 4 + SOFTMAX_ROWS * 8
+    value = nbytes * world / (ms * 1e-3) / 1e9
+    peaks = _peaks()
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        orc = oracle.default()
+        xs = x[:256].double().cpu().numpy()
+        t0 = time.perf_counter()
+        for r in range(xs.shape[0]):
+            orc.online_softmax_stats(xs[r], SOFTMAX_COLS)
+        dt = time.perf_counter() - t0
+        cpu = {"value": xs.size * 4 / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"256 of {SOFTMAX_ROWS} rows, fp64, {dt:.2f} s"}
+    line = {
+        "metric": "online softmax statistics, GB/s of rows read (fp32)", "value": value,
+        "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"score_rows_{SOFTMAX_ROWS}x{SOFTMAX_COLS}_f32",
+                   "shape": f"{SOFTMAX_ROWS} rows x {SOFTMAX_COLS} fp32, N(0,1)*5, seed {SOFTMAX_SEED}",
+                   "l2": "inputs exceed L2 (512 MiB)"},
+        "roofline": {"kernel": "online_softmax_stats", "bound": "hbm", "achieved": value,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": value / peaks["hbm_gbs"],
+                     "traffic": None},
+        "e2e": None, "gpu_launches": args.steps, "clocks": clk, "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -418,7 +489,12 @@ def main():
                     help="skip the end-to-end host-buffer loop (profiling runs)")
     ap.add_argument("--cpu-heads", type=int, default=4,
                     help="heads of the workload the oracle baseline times")
+    ap.add_argument("--kernel", choices=["attention", "online_softmax"], default="attention",
+                    help="the attention step (default) or the standalone online-softmax "
+                         "statistics kernel")
     args = ap.parse_args()
+    if args.kernel == "online_softmax":
+        return run_online_softmax(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -9,4 +9,5 @@ from .api import (FAError, FlashAttention, alloc_workspace, fa_backward,  # noqa
                   fa_backward_dkdv, fa_backward_dq, fa_backward_grads, fa_backward_noalloc,
                   fa_backward_preprocess,
                   fa_backward_workspace_size, fa_forward, fa_get_device_status,
+                  fa_online_softmax_stats,
                   fa_selftest_mma, flash_attention, lib, status_string, version)

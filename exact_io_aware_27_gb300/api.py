@@ -46,6 +46,7 @@ SIGNATURES = {
                                _P]),
     "fa_backward_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P,
                                  _P, _P]),
+    "fa_online_softmax_stats": (_I, [_P, ctypes.c_longlong, ctypes.c_longlong, _P, _P, _P]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_get_device_status": (_I, [ctypes.POINTER(_I)]),
     "fa_version": (_I, []),
@@ -236,6 +237,22 @@ def fa_backward_grads(Q, K, V, dO, workspace, causal=False, scale=None, dQ=None,
                                  workspace.numel(), _stream(Q, stream))
     _check("fa_backward_grads", rc)
     return dQ, dK, dV
+
+
+def fa_online_softmax_stats(x: torch.Tensor, m=None, l=None, stream=None):
+    """(m, l) per row of the fp32 CUDA matrix x [rows, cols]: m = row max,
+    l = sum exp(x - m) ("05_flash_attention.py", online_softmax_stats)."""
+    if not isinstance(x, torch.Tensor) or x.dim() != 2 or x.dtype != torch.float32:
+        raise ValueError("x must be a 2-D float32 tensor")
+    if not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA tensor")
+    rows, cols = x.shape
+    m = torch.empty(rows, dtype=torch.float32, device=x.device) if m is None else m
+    l = torch.empty(rows, dtype=torch.float32, device=x.device) if l is None else l
+    rc = lib().fa_online_softmax_stats(x.data_ptr(), rows, cols, m.data_ptr(), l.data_ptr(),
+                                       _stream(x, stream))
+    _check("fa_online_softmax_stats", rc)
+    return m, l
 
 
 def fa_get_device_status() -> int:

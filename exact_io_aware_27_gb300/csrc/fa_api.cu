@@ -307,6 +307,19 @@ int fa_backward(const void* Q, const void* K, const void* V, const void* O, cons
   return from_cuda(e);
 }
 
+int fa_online_softmax_stats(const float* x, long long rows, long long cols, float* m, float* l,
+                            void* stream) {
+  if (!x || !m || !l || rows < 1 || cols < 1) return FA_ERR_INVALID_ARG;
+  if (rows > (1LL << 40) || cols > (1LL << 40)) return FA_ERR_INVALID_ARG;
+  if (!aligned(x, 4) || !aligned(m, 4) || !aligned(l, 4)) return FA_ERR_MISALIGNED;
+  const Range rx = range_of(x, (size_t)rows * (size_t)cols * 4);
+  const Range rm = range_of(m, (size_t)rows * 4), rl = range_of(l, (size_t)rows * 4);
+  if (overlap(rx, rm) || overlap(rx, rl) || overlap(rm, rl)) return FA_ERR_INVALID_ARG;
+  int rc = check_device();
+  if (rc != FA_OK) return rc;
+  return from_cuda(launch_softmax_stats(x, rows, cols, m, l, static_cast<cudaStream_t>(stream)));
+}
+
 int fa_get_device_status(int* status_out) {
   if (!status_out) return FA_ERR_INVALID_ARG;
   unsigned int f = 0, b = 0;

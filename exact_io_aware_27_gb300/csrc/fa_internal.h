@@ -60,6 +60,10 @@ cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t s);
 // dK, dV and dQ in one launch (the two passes' CTAs interleaved).
 cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t s);
 
+// Online softmax statistics of fp32 rows (m, l per row).
+cudaError_t launch_softmax_stats(const float* x, long long rows, long long cols, float* m,
+                                 float* l, cudaStream_t s);
+
 // Read-and-clear of each translation unit's device status word.
 cudaError_t forward_read_status(unsigned int* out);
 cudaError_t bwd_read_status(unsigned int* out);

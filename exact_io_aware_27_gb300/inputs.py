@@ -90,3 +90,11 @@ def sample_indices(count: int, k: int, seed: int):
     g.manual_seed(int(seed))
     k = min(k, count)
     return torch.randperm(count, generator=g)[:k].sort().values.tolist()
+
+
+def score_rows(rows: int, cols: int, seed: int, std: float = 5.0) -> torch.Tensor:
+    """fp32 [rows, cols] standard normals times `std` from a seeded CPU generator
+    (the pages' online-softmax demo draws randn(10) * 5)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    return torch.randn(rows, cols, generator=g, dtype=torch.float32) * std

@@ -161,6 +161,23 @@ FA_API int fa_backward_noalloc(const void* Q, const void* K, const void* V, cons
                                int causal, float scale, void* dQ, void* dK, void* dV,
                                void* stream);
 
+/*
+ * Online softmax statistics ("05_flash_attention.py", online_softmax_stats;
+ * "Flash Attention" notes, section 1.1), the building block of the forward pass
+ * on its own: for each row of the row-major fp32 matrix x [rows, cols] (device
+ * memory), m[r] = max_j x[r, j] and l[r] = sum_j exp(x[r, j] - m[r]), computed in
+ * one pass over x with a running maximum and a rescaled sum. m[r] + log l[r] is
+ * the row's logsumexp and exp(x[r, j] - m[r]) / l[r] its softmax. Entries may be
+ * -inf; a row of -inf only gives m = -inf, l = 0. m and l are fp32 [rows]
+ * (device memory, caller owned, not overlapping x or each other); x is read
+ * once (16-byte loads when x is 16-byte aligned and cols % 4 == 0). Requires
+ * rows, cols >= 1 and 4-byte aligned pointers. The pages' block size only fixes
+ * the order of the updates, not the result, so it is not an argument here. One
+ * kernel launch on `stream`. Returns FA_OK or a negative fa_status.
+ */
+FA_API int fa_online_softmax_stats(const float* x, long long rows, long long cols, float* m,
+                                   float* l, void* stream);
+
 /* A static, human-readable name for a status code. Never NULL. */
 FA_API const char* fa_status_string(int status);
 

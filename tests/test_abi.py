@@ -130,3 +130,15 @@ def test_selftest_argument_errors(lib):
     assert lib.fa_selftest_mma(7, FAKE, FAKE, FAKE, None) == -1
     assert lib.fa_selftest_mma(0, None, FAKE, FAKE, None) == -1
     assert lib.fa_selftest_mma(0, FAKE + 2, FAKE, FAKE, None) == -3
+
+
+def test_online_softmax_argument_errors(lib):
+    f = lib.fa_online_softmax_stats
+    x, m, l = FAKE, FAKE + (1 << 24), FAKE + (2 << 24)
+    assert f(None, 4, 8, m, l, None) == api.FA_ERR_INVALID_ARG
+    assert f(x, 4, 8, None, l, None) == api.FA_ERR_INVALID_ARG
+    assert f(x, 0, 8, m, l, None) == api.FA_ERR_INVALID_ARG
+    assert f(x, 4, 0, m, l, None) == api.FA_ERR_INVALID_ARG
+    assert f(x + 2, 4, 8, m, l, None) == api.FA_ERR_MISALIGNED
+    assert f(x, 4, 8, x + 16, l, None) == api.FA_ERR_INVALID_ARG  # m inside x
+    assert f(x, 4, 8, m, m + 8, None) == api.FA_ERR_INVALID_ARG   # l overlaps m

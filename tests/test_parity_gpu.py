@@ -223,6 +223,26 @@ def test_autograd_wrapper_matches_direct_calls():
     assert torch.equal(k.grad, dK) and torch.equal(v.grad, dV) and torch.equal(q.grad, dQ)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_autograd_squared_output_loss(causal):
+    """The user-level workflow of the pages' backward demo ("05_flash_attention.py",
+    demo_backward: loss = sum of O squared, gradients by autograd) through the torch
+    wrapper on the GPU, checked against the oracle's gradients for the same upstream
+    gradient dO = 2 O (exact in bf16)."""
+    import oracle
+    Q, K, V, _ = wl.attention_inputs(2, 3, 70, 70, 64, seed=7750)
+    q, k, v = (t.cuda().requires_grad_(True) for t in (Q, K, V))
+    out = fa.flash_attention(q, k, v, causal)
+    loss = out.float().pow(2).sum()
+    loss.backward()
+    torch.cuda.synchronize()
+    dO = parity.f64(2 * out.detach().float().cpu())
+    dQ, dK, dV, _ = oracle.backward(parity.f64(Q), parity.f64(K), parity.f64(V), dO, causal)
+    for name, g, r in (("dQ", q.grad, dQ), ("dK", k.grad, dK), ("dV", v.grad, dV)):
+        err = parity.rel_fro(parity.f64(g.cpu()), r)
+        assert err <= parity.GRAD_REL, f"{name} relative Frobenius error {err:.3e}"
+
+
 def test_stage_entry_points_match_fa_backward():
     B, H, n, m, d = 1, 2, 300, 300, 128
     Q, K, V, dO = (t.cuda() for t in wl.attention_inputs(B, H, n, m, d, seed=7800))
