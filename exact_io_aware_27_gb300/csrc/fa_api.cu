@@ -6,6 +6,7 @@
 
 #include "fa.h"
 #include "fa_internal.h"
+#include "sm103.cuh"
 
 namespace fa {
 
@@ -325,7 +326,10 @@ int fa_get_device_status(int* status_out) {
   unsigned int f = 0, b = 0;
   if (forward_read_status(&f) != cudaSuccess || bwd_read_status(&b) != cudaSuccess)
     return FA_ERR_CUDA;
-  *status_out = ((f | b) & 1u) ? FA_ERR_DEVICE_TIMEOUT : FA_OK;
+  const unsigned int bits = f | b;
+  *status_out = (bits & kDeviceTimeoutBit)  ? FA_ERR_DEVICE_TIMEOUT
+                : (bits & kDeviceLayoutBit) ? FA_ERR_UNSUPPORTED_DEVICE
+                                            : FA_OK;
   return FA_OK;
 }
 

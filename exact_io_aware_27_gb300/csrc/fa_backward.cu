@@ -176,7 +176,7 @@ struct KvCfg {
   static constexpr int B_EPI = B_SF + 8;      // dK, dV read out of TMEM (256 arrivals)
   static constexpr int B_DRAIN = B_SF + 9;
   static constexpr int NBAR = B_DRAIN + 1;
-  static constexpr int SMEM = OFF_BAR + NBAR * 8 + 1024;
+  static constexpr int SMEM = OFF_BAR + NBAR * 8;
   // TMEM columns: K as bf16 pairs, two 64-column S^T regions, the dP^T region,
   // dV, dK. Group w keeps P^T over [32w, 32w + 16) and dS^T over
   // [32w + 16, 32w + 32) of the half's S^T region.
@@ -576,7 +576,7 @@ struct QCfg {
   static constexpr int B_EPI = B_SF + 7;       // dQ read out of TMEM (256 arrivals)
   static constexpr int B_DRAIN = B_SF + 8;
   static constexpr int NBAR = B_DRAIN + 1;
-  static constexpr int SMEM = OFF_BAR + NBAR * 8 + 1024;
+  static constexpr int SMEM = OFF_BAR + NBAR * 8;
   // TMEM columns: Q and dO as bf16 pairs; for half h of the key block S_h at
   // COL_S + 64h (then dS_h as bf16 pairs over its first 32 columns) and dP_h at
   // COL_DP + 64h; dQ.
@@ -899,6 +899,16 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const __nv_bfloat16* __
   }
 }
 
+// Shared memory of the gradient kernel: the larger of the two passes' layouts,
+// then the TMEM address slot and the abort word.
+template <int D>
+struct BwdSmem {
+  static constexpr int PASSES = KvCfg<D>::SMEM > QCfg<D>::SMEM ? KvCfg<D>::SMEM : QCfg<D>::SMEM;
+  static constexpr int CTL = (PASSES + 7) / 8 * 8;
+  static constexpr int BYTES = CTL + 8;
+  static_assert(BYTES <= 232448, "shared memory budget");
+};
+
 // The gradient kernel: one CTA per SM (persistent). The n_kv key blocks and then
 // the n_dq query blocks are dealt out in rounds of P = grid size items (CTA c takes
 // snake_item(r, c, P) of round r), so that each CTA runs its share of the dK/dV
@@ -910,20 +920,31 @@ __global__ void __launch_bounds__(384, 1)
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                const __grid_constant__ CUtensorMap tmNL2, const __grid_constant__ CUtensorMap tmND,
                const KvParams kp, const DqParams qp, int n_kv, int n_dq) {
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ uint32_t tmem_slot;
-  __shared__ uint32_t abort_word;
-  uint8_t* smem = align1024(smem_raw);
-  const WaitCtx wc{&abort_word, &g_bwd_status};
-  if (threadIdx.x == 0) abort_word = 0u;
+  // No static shared memory: the dynamic region then starts on a 1024-byte
+  // boundary, which the 128-byte swizzle of the tiles needs and which the layouts
+  // assume (they leave no room to align by hand). A kernel that finds another
+  // placement reports it and does nothing.
+  extern __shared__ uint8_t smem_dyn[];
+  if ((smem_u32(smem_dyn) & 1023u) != 0u) {
+    if (threadIdx.x == 0) atomicOr(&g_bwd_status, kDeviceLayoutBit);
+    return;
+  }
+  // align1024 is the identity here; it makes the base a run-time value. With the
+  // base known at compile time the generated code ran about 10% slower on GB300.
+  uint8_t* smem = align1024(smem_dyn);
+  constexpr int kCtl = BwdSmem<D>::CTL;  // two words after both passes' layouts
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kCtl);
+  uint32_t* abort_word = tmem_slot + 1;
+  const WaitCtx wc{abort_word, &g_bwd_status};
+  if (threadIdx.x == 0) *abort_word = 0u;
   if ((threadIdx.x >> 5) == 1) {
-    tmem_alloc(&tmem_slot, 512);
+    tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = tmem_slot;
+  const uint32_t tmem = *tmem_slot;
 
   const int P = gridDim.x, c = blockIdx.x;
   // Each list is dealt separately; the query blocks in reverse CTA order, so that
@@ -984,7 +1005,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, bool with_kv, bool with_dq, cudaStrea
   qp.group = heads_per_group(a.BH, qp.qtiles);
   const int n_kv = with_kv ? kp.ktiles * a.BH : 0;
   const int n_dq = with_dq ? qp.qtiles * a.BH : 0;
-  constexpr int smem = KC::SMEM > QC::SMEM ? KC::SMEM : QC::SMEM;
+  constexpr int smem = BwdSmem<D>::BYTES;
   cudaError_t e =
       cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;

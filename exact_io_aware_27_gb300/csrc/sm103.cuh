@@ -16,6 +16,9 @@ namespace fa {
 #define FA_DEV __device__ __forceinline__
 
 constexpr unsigned int kDeviceTimeoutBit = 1u;
+// Set by a kernel that found its dynamic shared memory at an address its layout
+// does not allow (it then returns before touching anything).
+constexpr unsigned int kDeviceLayoutBit = 2u;
 constexpr long long kWaitMaxCycles = 4000000000ll;  // ~2 s at 2 GHz
 constexpr uint32_t kWaitMaxPolls = 1u << 28;
 

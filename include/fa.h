@@ -183,8 +183,9 @@ FA_API const char* fa_status_string(int status);
 
 /*
  * Reads the device status word of the current device into *status_out
- * (FA_OK, or FA_ERR_DEVICE_TIMEOUT if a kernel gave up waiting since the last
- * read) and clears it. Synchronises with the device. Returns FA_OK or
+ * (FA_OK; FA_ERR_DEVICE_TIMEOUT if a kernel gave up waiting since the last
+ * read; FA_ERR_UNSUPPORTED_DEVICE if a kernel found its shared memory placed
+ * other than on a 1024-byte boundary and returned without work) and clears it. Synchronises with the device. Returns FA_OK or
  * FA_ERR_CUDA / FA_ERR_INVALID_ARG.
  */
 FA_API int fa_get_device_status(int* status_out);
