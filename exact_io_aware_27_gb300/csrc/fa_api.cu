@@ -71,7 +71,7 @@ int check_sizes(int B, int H, int n, int m, int d) {
   if (B < 1 || H < 1 || n < 1 || m < 1) return FA_ERR_INVALID_ARG;
   if (n > kMaxSeq || m > kMaxSeq) return FA_ERR_INVALID_ARG;
   if ((long long)B * H > 65535) return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED_HEAD_DIM;
+  if (d < 8 || d > 128 || d % 8 != 0) return FA_ERR_UNSUPPORTED_HEAD_DIM;
   return FA_OK;
 }
 
@@ -204,7 +204,7 @@ const char* fa_status_string(int status) {
   switch (status) {
     case FA_OK: return "ok";
     case FA_ERR_INVALID_ARG: return "invalid argument";
-    case FA_ERR_UNSUPPORTED_HEAD_DIM: return "unsupported head dimension (need 64 or 128)";
+    case FA_ERR_UNSUPPORTED_HEAD_DIM: return "unsupported head dimension (need a multiple of 8 from 8 to 128)";
     case FA_ERR_MISALIGNED: return "misaligned pointer";
     case FA_ERR_UNSUPPORTED_DEVICE: return "unsupported device (need compute capability 10.3)";
     case FA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";

@@ -195,6 +195,7 @@ struct KvCfg {
 struct KvParams {
   __nv_bfloat16 *dK, *dV;
   int n, m, n_pad, BH, causal, ktiles, group;
+  int d;  // head dimension (<= D; the tiles' columns past d are zero)
   float scale, scale_log2;
 };
 
@@ -233,13 +234,15 @@ __device__ __forceinline__ void tile_row_to_tmem(const uint8_t* tile, int r, uin
   tmem_st_wait();
 }
 
-// Rows [r0, ...) of a TMEM accumulator (this thread's lane), scaled and stored as a
-// bf16 row of D values at dst (skipped when !store).
+// NCOL columns of a TMEM accumulator row (this thread's lane), scaled and stored
+// as bf16 at dst (skipped when !store); only the first `valid` columns are real
+// (the rest are the zero padding of a head dimension below the tile's).
 template <int D, int NCOL>
 __device__ __forceinline__ void tmem_row_out(uint32_t col, float mul, __nv_bfloat16* dst,
-                                             bool store) {
+                                             bool store, int valid) {
 #pragma unroll
   for (int c = 0; c < NCOL / 32; ++c) {
+    if (32 * c >= valid) break;  // warp-uniform
     uint32_t o[32];
     tmem_ld32(col + 32 * c, o);
     tmem_ld_wait();
@@ -250,10 +253,9 @@ __device__ __forceinline__ void tmem_row_out(uint32_t col, float mul, __nv_bfloa
       wv[e] = pack_bf16(__uint_as_float(o[2 * e]) * mul, __uint_as_float(o[2 * e + 1]) * mul);
     if (store) {
       uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
-      d4[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-      d4[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
-      d4[2] = make_uint4(wv[8], wv[9], wv[10], wv[11]);
-      d4[3] = make_uint4(wv[12], wv[13], wv[14], wv[15]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (32 * c + 8 * j < valid) d4[j] = make_uint4(wv[4 * j], wv[4 * j + 1], wv[4 * j + 2], wv[4 * j + 3]);
     }
   }
 }
@@ -459,7 +461,7 @@ __device__ __forceinline__ void dkdv_run(const CUtensorMap& tmQ, const CUtensorM
       if (!warp_wait(&bar[C::B_ACC + (a & 1)], (a >> 1) & 1, wc)) return false;
       tc_fence_after();
       const int kg = pks + krow;
-      tmem_row_out<D, D>(acc_col, acc_mul, out + ((size_t)pbh * p.m + kg) * D, kg < p.m);
+      tmem_row_out<D, D>(acc_col, acc_mul, out + ((size_t)pbh * p.m + kg) * p.d, kg < p.m, p.d);
       tc_fence_before();
       mbar_arrive(&bar[C::B_EPI]);
       return true;
@@ -474,7 +476,7 @@ __device__ __forceinline__ void dkdv_run(const CUtensorMap& tmQ, const CUtensorM
           const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
           for (int c = 0; c < D / 8; ++c)
-            reinterpret_cast<uint4*>(out + ((size_t)bh * p.m + kg) * D)[c] = z;
+            if (8 * c < p.d) reinterpret_cast<uint4*>(out + ((size_t)bh * p.m + kg) * p.d)[c] = z;
         }
         continue;
       }
@@ -596,6 +598,7 @@ struct DqParams {
   __nv_bfloat16* dQ;
   const float *nD, *nL2;
   int n, m, n_pad, BH, causal, qtiles, group;
+  int d;  // head dimension (<= D; the tiles' columns past d are zero)
   float scale, scale_log2;
 };
 
@@ -773,7 +776,8 @@ __device__ __forceinline__ void dq_run(const CUtensorMap& tmQ, const CUtensorMap
       if (!warp_wait(&bar[C::B_ACC], a & 1, wc)) return false;
       tc_fence_after();
       tmem_row_out<D, D / 2>(tl + C::COL_DQ + h * (D / 2), p.scale,
-                             p.dQ + ((size_t)pbh * p.n + pq) * D + h * (D / 2), pq < p.n);
+                             p.dQ + ((size_t)pbh * p.n + pq) * p.d + h * (D / 2), pq < p.n,
+                             p.d - h * (D / 2));
       tc_fence_before();
       mbar_arrive(&bar[C::B_EPI]);
       return true;
@@ -787,7 +791,8 @@ __device__ __forceinline__ void dq_run(const CUtensorMap& tmQ, const CUtensorMap
           const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
           for (int c = 0; c < D / 16; ++c)
-            reinterpret_cast<uint4*>(p.dQ + ((size_t)bh * p.n + q) * D + h * (D / 2))[c] = z;
+            if (h * (D / 2) + 8 * c < p.d)
+              reinterpret_cast<uint4*>(p.dQ + ((size_t)bh * p.n + q) * p.d + h * (D / 2))[c] = z;
         }
         continue;
       }
@@ -869,7 +874,7 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const __nv_bfloat16* __
                                                          const float* __restrict__ L,
                                                          float* __restrict__ ws_nD,
                                                          float* __restrict__ ws_nL2, int n,
-                                                         int n_pad, long long rows) {
+                                                         int n_pad, int d, long long rows) {
   constexpr int LPR = D / 8;     // lanes per row (8 bf16 per lane)
   constexpr int RPW = 32 / LPR;  // rows per warp step
   const int lane = threadIdx.x & 31;
@@ -881,8 +886,8 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const __nv_bfloat16* __
     const long long bh = r / n_pad;
     const int q = (int)(r - bh * n_pad);
     float acc = 0.f;
-    if (q < n) {
-      const size_t off = ((size_t)bh * n + q) * D;
+    if (q < n && 8 * sub < d) {
+      const size_t off = ((size_t)bh * n + q) * d;
       const uint4 a = reinterpret_cast<const uint4*>(O + off)[sub];
       const uint4 b = reinterpret_cast<const uint4*>(dO + off)[sub];
       acc = bf16_lo(a.x) * bf16_lo(b.x) + bf16_hi(a.x) * bf16_hi(b.x) +
@@ -971,10 +976,11 @@ cudaError_t launch_bwd_d(const BwdArgs& a, bool with_kv, bool with_dq, cudaStrea
   static_assert(KC::THREADS == QC::THREADS, "the passes share the launch");
   CUtensorMap mq, mk, mv, mdo, ml2, md;
   // Q and dO, -L2 and -D travel in 64-row pieces; K and V in 128-row tiles.
-  if (make_bf16_head_map(&mq, a.Q, a.BH, a.n, D, 64) != CUDA_SUCCESS ||
-      make_bf16_head_map(&mk, a.K, a.BH, a.m, D, KC::BN) != CUDA_SUCCESS ||
-      make_bf16_head_map(&mv, a.V, a.BH, a.m, D, KC::BN) != CUDA_SUCCESS ||
-      make_bf16_head_map(&mdo, a.dO, a.BH, a.n, D, 64) != CUDA_SUCCESS ||
+  // Rows of d values; the 64-column boxes read zeros past d.
+  if (make_bf16_head_map(&mq, a.Q, a.BH, a.n, a.d, 64) != CUDA_SUCCESS ||
+      make_bf16_head_map(&mk, a.K, a.BH, a.m, a.d, KC::BN) != CUDA_SUCCESS ||
+      make_bf16_head_map(&mv, a.V, a.BH, a.m, a.d, KC::BN) != CUDA_SUCCESS ||
+      make_bf16_head_map(&mdo, a.dO, a.BH, a.n, a.d, 64) != CUDA_SUCCESS ||
       make_f32_row_map(&ml2, a.ws_nL2, a.BH, a.n_pad, 64) != CUDA_SUCCESS ||
       make_f32_row_map(&md, a.ws_nD, a.BH, a.n_pad, 64) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
@@ -986,6 +992,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, bool with_kv, bool with_dq, cudaStrea
   kp.n_pad = a.n_pad;
   kp.BH = a.BH;
   kp.causal = a.causal;
+  kp.d = a.d;
   kp.scale = a.scale;
   kp.scale_log2 = a.scale * kLog2e;
   kp.ktiles = ceil_div(a.m, KC::BN);
@@ -999,6 +1006,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, bool with_kv, bool with_dq, cudaStrea
   qp.n_pad = a.n_pad;
   qp.BH = a.BH;
   qp.causal = a.causal;
+  qp.d = a.d;
   qp.scale = a.scale;
   qp.scale_log2 = a.scale * kLog2e;
   qp.qtiles = ceil_div(a.n, QC::BM);
@@ -1029,28 +1037,31 @@ int grid_for(long long work_items, int per_block) {
 
 cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t s) {
   const long long rows = (long long)a.BH * a.n_pad;
-  const int grid = grid_for(rows / (a.d == 128 ? 2 : 4), 8);  // warp steps, 8 warps a block
-  if (a.d == 128)
+  const bool wide = a.d > 64;
+  const int grid = grid_for(rows / (wide ? 2 : 4), 8);  // warp steps, 8 warps a block
+  if (wide)
     preprocess_kernel<128><<<grid, 256, 0, s>>>(
         static_cast<const __nv_bfloat16*>(a.O), static_cast<const __nv_bfloat16*>(a.dO), a.L,
-        a.ws_nD, a.ws_nL2, a.n, a.n_pad, rows);
+        a.ws_nD, a.ws_nL2, a.n, a.n_pad, a.d, rows);
   else
     preprocess_kernel<64><<<grid, 256, 0, s>>>(
         static_cast<const __nv_bfloat16*>(a.O), static_cast<const __nv_bfloat16*>(a.dO), a.L,
-        a.ws_nD, a.ws_nL2, a.n, a.n_pad, rows);
+        a.ws_nD, a.ws_nL2, a.n, a.n_pad, a.d, rows);
   return cudaGetLastError();
 }
 
+// Head dimensions up to 64 run the 64-column kernels, larger ones the 128-column
+// kernels (columns past d read as zeros).
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t s) {
-  return a.d == 128 ? launch_bwd_d<128>(a, true, false, s) : launch_bwd_d<64>(a, true, false, s);
+  return a.d > 64 ? launch_bwd_d<128>(a, true, false, s) : launch_bwd_d<64>(a, true, false, s);
 }
 
 cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t s) {
-  return a.d == 128 ? launch_bwd_d<128>(a, false, true, s) : launch_bwd_d<64>(a, false, true, s);
+  return a.d > 64 ? launch_bwd_d<128>(a, false, true, s) : launch_bwd_d<64>(a, false, true, s);
 }
 
 cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t s) {
-  return a.d == 128 ? launch_bwd_d<128>(a, true, true, s) : launch_bwd_d<64>(a, true, true, s);
+  return a.d > 64 ? launch_bwd_d<128>(a, true, true, s) : launch_bwd_d<64>(a, true, true, s);
 }
 
 cudaError_t bwd_read_status(unsigned int* out) {

@@ -82,6 +82,7 @@ struct FwdParams {
   __nv_bfloat16* O;
   float* L;
   int n, m, BH, causal, num_pairs, group;
+  int d;             // head dimension (<= D; the tiles' columns past d are zero)
   float scale_log2;  // scale * log2(e)
 };
 
@@ -366,9 +367,10 @@ __global__ void __launch_bounds__(384, 1)
     if (ok && nh_t > 0 && warp_wait(&bar[C::B_PVD + t], 0, wc)) {
       tc_fence_after();
       const float inv_l = 1.f / l_run;
-      __nv_bfloat16* orow = p.O + ((size_t)bh * p.n + qg) * D;
+      __nv_bfloat16* orow = p.O + ((size_t)bh * p.n + qg) * p.d;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
+        if (32 * c >= p.d) break;  // columns past d are zero padding
         uint32_t o[32];
         tmem_ld32(ocol + 32 * c, o);
         tmem_ld_wait();
@@ -379,10 +381,9 @@ __global__ void __launch_bounds__(384, 1)
           w[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
         if (qg < p.n) {
           uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
-          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-          dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
-          dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (32 * c + 8 * j < p.d) dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
         }
       }
       if (qg < p.n) p.L[(size_t)bh * p.n + qg] = (m_ref + lg2(l_run)) * kLn2;
@@ -401,9 +402,10 @@ template <int D>
 cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
   using C = FwdCfg<D>;
   CUtensorMap mq, mk, mv;
-  if (make_bf16_head_map(&mq, a.Q, a.BH, a.n, D, C::BM) != CUDA_SUCCESS ||
-      make_bf16_head_map(&mk, a.K, a.BH, a.m, D, C::BN) != CUDA_SUCCESS ||
-      make_bf16_head_map(&mv, a.V, a.BH, a.m, D, C::BN) != CUDA_SUCCESS)
+  // Rows of d values; the 64-column boxes read zeros past d.
+  if (make_bf16_head_map(&mq, a.Q, a.BH, a.n, a.d, C::BM) != CUDA_SUCCESS ||
+      make_bf16_head_map(&mk, a.K, a.BH, a.m, a.d, C::BN) != CUDA_SUCCESS ||
+      make_bf16_head_map(&mv, a.V, a.BH, a.m, a.d, C::BN) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   FwdParams p;
   p.O = static_cast<__nv_bfloat16*>(a.O);
@@ -412,6 +414,7 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
   p.m = a.m;
   p.BH = a.BH;
   p.causal = a.causal;
+  p.d = a.d;
   p.num_pairs = ceil_div(a.n, C::TILES * C::BM);
   p.group = heads_per_group(a.BH, p.num_pairs);
   p.scale_log2 = a.scale * 1.44269504088896340736f;
@@ -426,7 +429,7 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_forward(const FwdArgs& a, cudaStream_t s) {
-  return a.d == 128 ? launch_fwd_d<128>(a, s) : launch_fwd_d<64>(a, s);
+  return a.d > 64 ? launch_fwd_d<128>(a, s) : launch_fwd_d<64>(a, s);
 }
 
 cudaError_t forward_read_status(unsigned int* out) {

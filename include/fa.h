@@ -17,7 +17,9 @@
  * Layouts. Every tensor is dense and row-major ("contiguous"):
  *   Q, dO, O, dQ : bf16 [B, H, n, d]        K, V, dK, dV : bf16 [B, H, m, d]
  *   L            : fp32 [B, H, n]           (natural log)
- * d must be 64 or 128. n, m, B, H >= 1; B*H <= 65535 and n, m <= 2^24.
+ * d is a multiple of 8 from 8 to 128 (64 and 128 are the tuned cases; other
+ * values run the next larger of the two with the extra columns read as zeros,
+ * which changes no result). n, m, B, H >= 1; B*H <= 65535 and n, m <= 2^24.
  * scale must be finite and > 0 (1/sqrt(d) is the usual choice).
  * All arithmetic accumulates in fp32; O, dQ, dK, dV are rounded to bf16
  * (round to nearest even).
@@ -55,7 +57,7 @@ extern "C" {
 typedef enum {
   FA_OK = 0,
   FA_ERR_INVALID_ARG = -1,          /* null pointer, bad size, bad scale, overlap */
-  FA_ERR_UNSUPPORTED_HEAD_DIM = -2, /* d not in {64, 128} */
+  FA_ERR_UNSUPPORTED_HEAD_DIM = -2, /* d not a multiple of 8 in [8, 128] */
   FA_ERR_MISALIGNED = -3,           /* a pointer breaks the alignment rules above */
   FA_ERR_UNSUPPORTED_DEVICE = -4,   /* current device is not compute capability 10.3 */
   FA_ERR_WORKSPACE_TOO_SMALL = -5,  /* workspace_bytes < fa_backward_workspace_size() */

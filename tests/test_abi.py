@@ -50,7 +50,8 @@ def test_workspace_size(lib):
     assert fa.fa_backward_workspace_size(1, 1, 128, 128, 128) == 128 * 2 * 4
     assert fa.fa_backward_workspace_size(1, 1, 129, 7, 128) == 256 * 2 * 4
     assert fa.fa_backward_workspace_size(1, 1, 0, 7, 128) == 0
-    assert fa.fa_backward_workspace_size(1, 1, 8, 7, 96) == 0
+    assert fa.fa_backward_workspace_size(1, 1, 8, 7, 96) == 128 * 2 * 4
+    assert fa.fa_backward_workspace_size(1, 1, 8, 7, 100) == 0  # unsupported d
 
 
 FAKE = 1 << 20  # an aligned non-null address; never dereferenced (validation fails first)
@@ -68,8 +69,8 @@ def test_forward_argument_errors(lib):
     assert _fwd(lib, m=-3) == api.FA_ERR_INVALID_ARG
     assert _fwd(lib, B=0) == api.FA_ERR_INVALID_ARG
     assert _fwd(lib, B=256, H=256) == api.FA_ERR_INVALID_ARG
-    assert _fwd(lib, d=96) == api.FA_ERR_UNSUPPORTED_HEAD_DIM
-    assert _fwd(lib, d=256) == api.FA_ERR_UNSUPPORTED_HEAD_DIM
+    for d in (0, 4, 12, 100, 136, 256):  # not a multiple of 8 in [8, 128]
+        assert _fwd(lib, d=d) == api.FA_ERR_UNSUPPORTED_HEAD_DIM
     assert _fwd(lib, scale=0.0) == api.FA_ERR_INVALID_ARG
     assert _fwd(lib, scale=-1.0) == api.FA_ERR_INVALID_ARG
     assert _fwd(lib, scale=float("nan")) == api.FA_ERR_INVALID_ARG
@@ -87,7 +88,8 @@ def test_forward_valid_arguments_reach_the_device_check(lib):
     import torch
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
-    assert _fwd(lib) in (api.FA_ERR_CUDA, api.FA_ERR_UNSUPPORTED_DEVICE)
+    for d in (8, 16, 32, 64, 96, 128):
+        assert _fwd(lib, d=d) in (api.FA_ERR_CUDA, api.FA_ERR_UNSUPPORTED_DEVICE)
 
 
 def test_backward_argument_errors(lib):
@@ -105,7 +107,8 @@ def test_backward_argument_errors(lib):
 
     assert bwd(dO=None) == api.FA_ERR_INVALID_ARG
     assert bwd(ws=None) == api.FA_ERR_INVALID_ARG
-    assert bwd(d=32) == api.FA_ERR_UNSUPPORTED_HEAD_DIM
+    assert bwd(d=20) == api.FA_ERR_UNSUPPORTED_HEAD_DIM
+    assert bwd(d=144) == api.FA_ERR_UNSUPPORTED_HEAD_DIM
     assert bwd(wsb=ws - 4) == api.FA_ERR_WORKSPACE_TOO_SMALL
     assert bwd(dK=base[7] + 2) == api.FA_ERR_MISALIGNED
     assert bwd(ws=base[9] + 4) == api.FA_ERR_MISALIGNED

@@ -94,6 +94,31 @@ def test_edge_shapes(B, H, n, m, d, causal):
     parity.check_heads(Q, K, V, dO, causal, got)
 
 
+# Head dimensions other than 64 and 128 (multiples of 8 up to 128) run the next
+# larger kernel on zero-filled columns. The first two are the shape of the
+# tiled-forward demo of "05_flash_attention.py" (n = 100, d = 32).
+OTHER_DIMS = [
+    # (B, H, n, m, d, causal)
+    (1, 1, 100, 100, 32, False),
+    (1, 1, 100, 100, 32, True),
+    (2, 3, 70, 70, 16, True),
+    (1, 2, 300, 257, 8, False),
+    (1, 1, 129, 200, 48, True),
+    (2, 1, 257, 257, 96, True),
+    (1, 1, 1, 1, 16, False),
+    (1, 1, 500, 500, 120, False),
+    (1, 1, 64, 64, 72, True),
+    (1, 1, 333, 1000, 24, False),
+]
+
+
+@pytest.mark.parametrize("B,H,n,m,d,causal", OTHER_DIMS)
+def test_other_head_dims(B, H, n, m, d, causal):
+    Q, K, V, dO = wl.attention_inputs(B, H, n, m, d, seed=7300 + n + 3 * m + d, qk_std=1.0)
+    got = parity.run_gpu(Q, K, V, dO, causal)
+    parity.check_heads(Q, K, V, dO, causal, got)
+
+
 def test_peaked_scores_and_custom_scale():
     # Q, K ~ 3 N(0,1): peaked softmax, large row maxima; non-default scale
     Q, K, V, dO = wl.attention_inputs(1, 2, 300, 500, 128, seed=7100, qk_std=3.0)
@@ -181,7 +206,8 @@ def _guarded(shape, dtype, fill):
     return buf, buf[guard:guard + numel].view(*shape), guard
 
 
-@pytest.mark.parametrize("d,causal", [(64, False), (128, True)])
+@pytest.mark.parametrize("d,causal", [(64, False), (128, True), (32, True), (96, False),
+                                     (8, False)])
 def test_outputs_written_exactly_in_bounds(d, causal):
     B, H, n, m = 2, 2, 201, 333
     Q, K, V, dO = (t.cuda() for t in wl.attention_inputs(B, H, n, m, d, seed=7500 + d))
@@ -226,11 +252,11 @@ def test_autograd_wrapper_matches_direct_calls():
 @pytest.mark.parametrize("causal", [False, True])
 def test_autograd_squared_output_loss(causal):
     """The user-level workflow of the pages' backward demo ("05_flash_attention.py",
-    demo_backward: loss = sum of O squared, gradients by autograd) through the torch
-    wrapper on the GPU, checked against the oracle's gradients for the same upstream
-    gradient dO = 2 O (exact in bf16)."""
+    demo_backward: n = 70, d = 16, loss = sum of O squared, gradients by autograd)
+    through the torch wrapper on the GPU, checked against the oracle's gradients for
+    the same upstream gradient dO = 2 O (exact in bf16)."""
     import oracle
-    Q, K, V, _ = wl.attention_inputs(2, 3, 70, 70, 64, seed=7750)
+    Q, K, V, _ = wl.attention_inputs(2, 3, 70, 70, 16, seed=7750)
     q, k, v = (t.cuda().requires_grad_(True) for t in (Q, K, V))
     out = fa.flash_attention(q, k, v, causal)
     loss = out.float().pow(2).sum()
