@@ -184,6 +184,14 @@ CUresult make_bf16_head_map(CUtensorMap* map, const void* base, int BH, int rows
                            dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+CUresult make_bf16_store_map(CUtensorMap* map, void* base, int BH, int rows, int d) {
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)BH};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)rows * d * 2};
+  const cuuint32_t box[3] = {32, 32, 1};
+  return encode_tensor_map(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
 CUresult make_f32_row_map(CUtensorMap* map, const void* base, int BH, int cols, int box_cols) {
   const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)BH};
   const cuuint64_t strides[1] = {(cuuint64_t)cols * 4};

@@ -159,7 +159,9 @@ struct KvCfg {
   static constexpr int OFF_R = 2 * TILE;         // the ring
   static constexpr int OFF_NL2 = OFF_R + STAGES * SLOT;      // [STAGES][64] fp32
   static constexpr int OFF_ND = OFF_NL2 + STAGES * 64 * 4;   // [STAGES][64] fp32
-  static constexpr int OFF_BAR = OFF_ND + STAGES * 64 * 4;
+  // dK / dV staging for the TMA stores, one area per compute warp
+  static constexpr int OFF_EPI = (OFF_ND + STAGES * 64 * 4 + 1023) / 1024 * 1024;
+  static constexpr int OFF_BAR = OFF_EPI + 8 * kStoreStageBytes;
   // barrier slots
   static constexpr int B_QF = 0;              // + slot: the slot's copies landed
   static constexpr int B_QE = STAGES;         // + slot: the slot may be refilled
@@ -234,37 +236,12 @@ __device__ __forceinline__ void tile_row_to_tmem(const uint8_t* tile, int r, uin
   tmem_st_wait();
 }
 
-// NCOL columns of a TMEM accumulator row (this thread's lane), scaled and stored
-// as bf16 at dst (skipped when !store); only the first `valid` columns are real
-// (the rest are the zero padding of a head dimension below the tile's).
-template <int D, int NCOL>
-__device__ __forceinline__ void tmem_row_out(uint32_t col, float mul, __nv_bfloat16* dst,
-                                             bool store, int valid) {
-#pragma unroll
-  for (int c = 0; c < NCOL / 32; ++c) {
-    if (32 * c >= valid) break;  // warp-uniform
-    uint32_t o[32];
-    tmem_ld32(col + 32 * c, o);
-    tmem_ld_wait();
-    reg_fence32(o);
-    uint32_t wv[16];
-#pragma unroll
-    for (int e = 0; e < 16; ++e)
-      wv[e] = pack_bf16(__uint_as_float(o[2 * e]) * mul, __uint_as_float(o[2 * e + 1]) * mul);
-    if (store) {
-      uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (32 * c + 8 * j < valid) d4[j] = make_uint4(wv[4 * j], wv[4 * j + 1], wv[4 * j + 2], wv[4 * j + 3]);
-    }
-  }
-}
-
 // Key blocks snake_item(r0 + t, c, P) (t < count) in launch order, by CTA c.
 template <int D>
 __device__ __forceinline__ void dkdv_run(const CUtensorMap& tmQ, const CUtensorMap& tmK,
                                          const CUtensorMap& tmV, const CUtensorMap& tmdO,
                                          const CUtensorMap& tmNL2, const CUtensorMap& tmND,
+                                         const CUtensorMap& tmdK, const CUtensorMap& tmdV,
                                          const KvParams& p, uint8_t* smem, uint32_t tmem,
                                          int r0, int c, int P, int count, const WaitCtx& wc) {
   using C = KvCfg<D>;
@@ -453,6 +430,8 @@ __device__ __forceinline__ void dkdv_run(const CUtensorMap& tmQ, const CUtensorM
     const uint32_t acc_col = tl + (w == 0 ? C::COL_DV : C::COL_DK);
     const float acc_mul = w == 0 ? 1.f : p.scale;
     __nv_bfloat16* const out = w == 0 ? p.dV : p.dK;
+    const CUtensorMap* const out_map = w == 0 ? &tmdV : &tmdK;
+    uint8_t* const stage = smem + C::OFF_EPI + (warp - 4) * kStoreStageBytes;
     int ru = 0, hu = 0, at = 0;
     int prev_bh = 0, prev_ks = 0;
     bool ok = true;
@@ -460,8 +439,8 @@ __device__ __forceinline__ void dkdv_run(const CUtensorMap& tmQ, const CUtensorM
     auto epilogue = [&](int a, int pbh, int pks) {
       if (!warp_wait(&bar[C::B_ACC + (a & 1)], (a >> 1) & 1, wc)) return false;
       tc_fence_after();
-      const int kg = pks + krow;
-      tmem_row_out<D, D>(acc_col, acc_mul, out + ((size_t)pbh * p.m + kg) * p.d, kg < p.m, p.d);
+      tmem_rows_store<D>(acc_col, acc_mul, stage, out_map, 0, pks + (warp & 3) * 32, p.m, pbh,
+                         p.d);
       tc_fence_before();
       mbar_arrive(&bar[C::B_EPI]);
       return true;
@@ -539,6 +518,7 @@ __device__ __forceinline__ void dkdv_run(const CUtensorMap& tmQ, const CUtensorM
       ++at;
     }
     if (ok && at >= 1) epilogue(at - 1, prev_bh, prev_ks);
+    if (lane == 0) bulk_wait_all();  // the stores have read their staging buffers
   }
 
   tc_fence_before();
@@ -566,7 +546,8 @@ struct QCfg {
   static constexpr int STAGES = (D == 128) ? 3 : 4;
   static constexpr int OFF_K = 0;              // ring: K_j (or the next block's Q)
   static constexpr int OFF_V = STAGES * TILE;  // ring: V_j (or the next block's dO)
-  static constexpr int OFF_BAR = 2 * STAGES * TILE;
+  static constexpr int OFF_EPI = 2 * STAGES * TILE;  // dQ staging, one area per compute warp
+  static constexpr int OFF_BAR = OFF_EPI + 8 * kStoreStageBytes;
   static constexpr int B_KVF = 0;              // + slot: the slot's copies landed
   static constexpr int B_KVE = STAGES;         // + slot: the slot may be refilled
   static constexpr int B_IN = 2 * STAGES;      // Q and dO rows in TMEM (256 arrivals)
@@ -606,7 +587,8 @@ struct DqParams {
 template <int D>
 __device__ __forceinline__ void dq_run(const CUtensorMap& tmQ, const CUtensorMap& tmK,
                                        const CUtensorMap& tmV, const CUtensorMap& tmdO,
-                                       const DqParams& p, uint8_t* smem, uint32_t tmem, int r0,
+                                       const CUtensorMap& tmdQ, const DqParams& p, uint8_t* smem,
+                                       uint32_t tmem, int r0,
                                        int c, int P, int skip, int count, const WaitCtx& wc) {
   using C = QCfg<D>;
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
@@ -771,13 +753,14 @@ __device__ __forceinline__ void dq_run(const CUtensorMap& tmQ, const CUtensorMap
     int ru = 0, gb = 0, at = 0;
     int prev_q = 0, prev_bh = 0;
     bool ok = true;
-    // dQ row of block a (head pbh, query pq): group h writes columns [h D/2, (h+1) D/2)
-    auto epilogue = [&](int a, int pbh, int pq) {
+    uint8_t* const stage = smem + C::OFF_EPI + (warp - 4) * kStoreStageBytes;
+    // dQ of block a (head pbh, first query pq0): group h writes columns
+    // [h D/2, (h+1) D/2) of the warp's 32 rows
+    auto epilogue = [&](int a, int pbh, int pq0) {
       if (!warp_wait(&bar[C::B_ACC], a & 1, wc)) return false;
       tc_fence_after();
-      tmem_row_out<D, D / 2>(tl + C::COL_DQ + h * (D / 2), p.scale,
-                             p.dQ + ((size_t)pbh * p.n + pq) * p.d + h * (D / 2), pq < p.n,
-                             p.d - h * (D / 2));
+      tmem_rows_store<D / 2>(tl + C::COL_DQ + h * (D / 2), p.scale, stage, &tmdQ, h * (D / 2),
+                             pq0 + (warp & 3) * 32, p.n, pbh, p.d - h * (D / 2));
       tc_fence_before();
       mbar_arrive(&bar[C::B_EPI]);
       return true;
@@ -848,13 +831,14 @@ __device__ __forceinline__ void dq_run(const CUtensorMap& tmQ, const CUtensorMap
         tc_fence_before();
         mbar_arrive(&bar[C::B_DSF + h]);
       }
-      prev_q = q;
+      prev_q = q0;
       prev_bh = bh;
       ru += 1 + nkb;
       gb += nkb;
       ++at;
     }
     if (ok && at >= 1) epilogue(at - 1, prev_bh, prev_q);
+    if (lane == 0) bulk_wait_all();  // the stores have read their staging buffers
   }
 
   tc_fence_before();
@@ -924,7 +908,9 @@ __global__ void __launch_bounds__(384, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                const __grid_constant__ CUtensorMap tmNL2, const __grid_constant__ CUtensorMap tmND,
-               const KvParams kp, const DqParams qp, int n_kv, int n_dq) {
+               const __grid_constant__ CUtensorMap tmdQ, const __grid_constant__ CUtensorMap tmdK,
+               const __grid_constant__ CUtensorMap tmdV, const KvParams kp, const DqParams qp,
+               int n_kv, int n_dq) {
   // No static shared memory: the dynamic region then starts on a 1024-byte
   // boundary, which the 128-byte swizzle of the tiles needs and which the layouts
   // assume (they leave no room to align by hand). A kernel that finds another
@@ -957,8 +943,10 @@ __global__ void __launch_bounds__(384, 1)
   int kv_rounds = 0, dq_rounds = 0;
   while (snake_item(kv_rounds, c, P) < n_kv) ++kv_rounds;
   while (snake_item(dq_rounds, P - 1 - c, P) < n_dq) ++dq_rounds;
-  if (kv_rounds > 0) dkdv_run<D>(tmQ, tmK, tmV, tmdO, tmNL2, tmND, kp, smem, tmem, 0, c, P, kv_rounds, wc);
-  if (dq_rounds > 0) dq_run<D>(tmQ, tmK, tmV, tmdO, qp, smem, tmem, 0, P - 1 - c, P, 0, dq_rounds, wc);
+  if (kv_rounds > 0)
+    dkdv_run<D>(tmQ, tmK, tmV, tmdO, tmNL2, tmND, tmdK, tmdV, kp, smem, tmem, 0, c, P, kv_rounds, wc);
+  if (dq_rounds > 0)
+    dq_run<D>(tmQ, tmK, tmV, tmdO, tmdQ, qp, smem, tmem, 0, P - 1 - c, P, 0, dq_rounds, wc);
 
   tc_fence_before();
   __syncthreads();
@@ -974,7 +962,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, bool with_kv, bool with_dq, cudaStrea
   using QC = QCfg<D>;
   static_assert(KC::BQ == QC::BM && KC::BN == QC::BN, "the passes share the tensor maps");
   static_assert(KC::THREADS == QC::THREADS, "the passes share the launch");
-  CUtensorMap mq, mk, mv, mdo, ml2, md;
+  CUtensorMap mq, mk, mv, mdo, ml2, md, mdq, mdk, mdv;
   // Q and dO, -L2 and -D travel in 64-row pieces; K and V in 128-row tiles.
   // Rows of d values; the 64-column boxes read zeros past d.
   if (make_bf16_head_map(&mq, a.Q, a.BH, a.n, a.d, 64) != CUDA_SUCCESS ||
@@ -982,7 +970,10 @@ cudaError_t launch_bwd_d(const BwdArgs& a, bool with_kv, bool with_dq, cudaStrea
       make_bf16_head_map(&mv, a.V, a.BH, a.m, a.d, KC::BN) != CUDA_SUCCESS ||
       make_bf16_head_map(&mdo, a.dO, a.BH, a.n, a.d, 64) != CUDA_SUCCESS ||
       make_f32_row_map(&ml2, a.ws_nL2, a.BH, a.n_pad, 64) != CUDA_SUCCESS ||
-      make_f32_row_map(&md, a.ws_nD, a.BH, a.n_pad, 64) != CUDA_SUCCESS)
+      make_f32_row_map(&md, a.ws_nD, a.BH, a.n_pad, 64) != CUDA_SUCCESS ||
+      make_bf16_store_map(&mdq, a.dQ, a.BH, a.n, a.d) != CUDA_SUCCESS ||
+      make_bf16_store_map(&mdk, a.dK, a.BH, a.m, a.d) != CUDA_SUCCESS ||
+      make_bf16_store_map(&mdv, a.dV, a.BH, a.m, a.d) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   KvParams kp;
   kp.dK = static_cast<__nv_bfloat16*>(a.dK);
@@ -1021,8 +1012,8 @@ cudaError_t launch_bwd_d(const BwdArgs& a, bool with_kv, bool with_dq, cudaStrea
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid = n_kv + n_dq < sms ? n_kv + n_dq : sms;
-  bwd_kernel<D><<<(unsigned)grid, KC::THREADS, smem, stream>>>(mq, mk, mv, mdo, ml2, md, kp, qp,
-                                                               n_kv, n_dq);
+  bwd_kernel<D><<<(unsigned)grid, KC::THREADS, smem, stream>>>(mq, mk, mv, mdo, ml2, md, mdq, mdk,
+                                                               mdv, kp, qp, n_kv, n_dq);
   return cudaGetLastError();
 }
 

@@ -56,7 +56,8 @@ struct FwdCfg {
   static constexpr int STAGES = (D == 128) ? 3 : 6;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = STAGES * TILE;
-  static constexpr int OFF_BAR = 2 * STAGES * TILE;
+  static constexpr int OFF_EPI = 2 * STAGES * TILE;  // O staging, one area per softmax warp
+  static constexpr int OFF_BAR = OFF_EPI + 8 * kStoreStageBytes;
   // barrier slots
   static constexpr int B_KVF = 0;                // + slot: the slot's copies landed
   static constexpr int B_KVE = STAGES;           // + slot: the slot may be refilled
@@ -106,7 +107,8 @@ __device__ __forceinline__ int tile_steps(int q0, int n, int m, int causal) {
 template <int D>
 __global__ void __launch_bounds__(384, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-               const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+               const FwdParams p) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -366,27 +368,12 @@ __global__ void __launch_bounds__(384, 1)
     // ------------------------------------------------------------ epilogue
     if (ok && nh_t > 0 && warp_wait(&bar[C::B_PVD + t], 0, wc)) {
       tc_fence_after();
-      const float inv_l = 1.f / l_run;
-      __nv_bfloat16* orow = p.O + ((size_t)bh * p.n + qg) * p.d;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        if (32 * c >= p.d) break;  // columns past d are zero padding
-        uint32_t o[32];
-        tmem_ld32(ocol + 32 * c, o);
-        tmem_ld_wait();
-        reg_fence32(o);
-        uint32_t w[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-          w[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
-        if (qg < p.n) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if (32 * c + 8 * j < p.d) dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-        }
-      }
+      // O / l as bf16 through the warp's staging area and TMA (rows past n and the
+      // zero columns past d are not written)
+      tmem_rows_store<D>(ocol, 1.f / l_run, smem + C::OFF_EPI + (warp - 4) * kStoreStageBytes,
+                         &tmO, 0, qs + t * C::BM + ((warp - 4) & 3) * 32, p.n, bh, p.d);
       if (qg < p.n) p.L[(size_t)bh * p.n + qg] = (m_ref + lg2(l_run)) * kLn2;
+      if (lane == 0) bulk_wait_all();  // the stores have read the staging buffers
     }
   }
 
@@ -401,11 +388,12 @@ __global__ void __launch_bounds__(384, 1)
 template <int D>
 cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
   using C = FwdCfg<D>;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   // Rows of d values; the 64-column boxes read zeros past d.
   if (make_bf16_head_map(&mq, a.Q, a.BH, a.n, a.d, C::BM) != CUDA_SUCCESS ||
       make_bf16_head_map(&mk, a.K, a.BH, a.m, a.d, C::BN) != CUDA_SUCCESS ||
-      make_bf16_head_map(&mv, a.V, a.BH, a.m, a.d, C::BN) != CUDA_SUCCESS)
+      make_bf16_head_map(&mv, a.V, a.BH, a.m, a.d, C::BN) != CUDA_SUCCESS ||
+      make_bf16_store_map(&mo, a.O, a.BH, a.n, a.d) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   FwdParams p;
   p.O = static_cast<__nv_bfloat16*>(a.O);
@@ -422,7 +410,7 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
       cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)p.num_pairs * (unsigned)a.BH;
-  fwd_kernel<D><<<grid, C::THREADS, C::SMEM, stream>>>(mq, mk, mv, p);
+  fwd_kernel<D><<<grid, C::THREADS, C::SMEM, stream>>>(mq, mk, mv, mo, p);
   return cudaGetLastError();
 }
 

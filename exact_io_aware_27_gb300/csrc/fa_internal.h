@@ -32,6 +32,9 @@ CUresult encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, cuuint32
 // head are zero-filled.
 CUresult make_bf16_head_map(CUtensorMap* map, const void* base, int BH, int rows, int d,
                             int box_rows);
+// bf16 [BH, rows, d] for the epilogues' stores: boxes of 32 columns x 32 rows
+// with 64-byte swizzle; rows and columns past the tensor are not written.
+CUresult make_bf16_store_map(CUtensorMap* map, void* base, int BH, int rows, int d);
 // fp32 [BH, cols] as a 2-D tensor, boxes of box_cols x 1, no swizzle.
 CUresult make_f32_row_map(CUtensorMap* map, const void* base, int BH, int cols, int box_cols);
 

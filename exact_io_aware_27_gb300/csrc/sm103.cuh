@@ -116,6 +116,23 @@ FA_DEV void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
+// Tiled 3-D store from shared memory, as a bulk async-group of the calling
+// thread. Rows and columns outside the tensor are not written. c0 follows the
+// load's alignment rule; no coordinate may be negative.
+FA_DEV void tma_store_3d(const CUtensorMap* map, const void* src, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+FA_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until at most N of this thread's bulk groups still read shared memory.
+template <int N>
+FA_DEV void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Waits until all of this thread's bulk groups are complete.
+FA_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 FA_DEV void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
@@ -124,7 +141,7 @@ FA_DEV void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0
       : "memory");
 }
 // Makes this thread's generic-proxy shared-memory writes visible to the async
-// proxy (tensor-core operand reads).
+// proxy (tensor-core operand reads, TMA stores).
 FA_DEV void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -345,6 +362,60 @@ FA_DEV void st_shared_v4(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c, uin
 FA_DEV uint8_t* align1024(uint8_t* p) {
   const uint32_t a = smem_u32(p);
   return p + (((a + 1023u) & ~1023u) - a);
+}
+
+// ------------------------------------------------------------------ epilogue stores
+// Bytes of one warp's staging area for tmem_rows_store (two buffers of 32 rows x
+// 32 bf16); the area must start on a 1024-byte boundary.
+constexpr int kStoreStageBytes = 2 * 2048;
+
+// Stores columns [0, NCOL) of this warp's 32 TMEM lanes (an fp32 accumulator at
+// `tcol`, times this lane's `mul`, rounded to bf16) to rows row0 .. row0 + 31 of
+// head bh and columns col0 + [0, NCOL) of a bf16 [BH, rows, d] tensor, through
+// `map` (boxes of 32 columns x 32 rows, 64-byte swizzle). Only the first
+// `valid_cols` columns are stored, and nothing when row0 >= nrows (the tensor's
+// rows). Each 32-column piece is written to one of the
+// warp's two staging buffers in `stage`, with the swizzle the map expects
+// (16-byte chunk k of row r at chunk k ^ ((r >> 1) & 3)), and lane 0 stores it
+// with one TMA copy; TMA leaves rows and columns outside the tensor untouched.
+// Lane 0 owns the copies: before `stage` holds anything else it must call
+// bulk_wait_read<0>() (or bulk_wait_all()).
+template <int NCOL>
+FA_DEV void tmem_rows_store(uint32_t tcol, float mul, uint8_t* stage, const CUtensorMap* map,
+                            int col0, int row0, int nrows, int bh, int valid_cols) {
+  if (row0 >= nrows) return;  // warp-uniform
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) bulk_wait_read<0>();  // copies of an earlier call
+  __syncwarp();
+#pragma unroll
+  for (int c = 0; c < NCOL / 32; ++c) {
+    if (32 * c >= valid_cols) break;  // warp-uniform
+    uint32_t o[32];
+    tmem_ld32(tcol + 32 * c, o);
+    tmem_ld_wait();
+    reg_fence32(o);
+    uint32_t w[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      w[e] = pack_bf16(__uint_as_float(o[2 * e]) * mul, __uint_as_float(o[2 * e + 1]) * mul);
+    uint8_t* buf = stage + (c & 1) * 2048;
+    if (c >= 2) {  // the copy of piece c - 2 has read this buffer
+      if (lane == 0) bulk_wait_read<1>();
+      __syncwarp();
+    }
+    const uint32_t row = smem_u32(buf) + lane * 64;
+    const uint32_t sw = (uint32_t)((lane >> 1) & 3);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      st_shared_v4(row + (((uint32_t)k ^ sw) << 4), w[4 * k], w[4 * k + 1], w[4 * k + 2],
+                   w[4 * k + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_3d(map, buf, col0 + 32 * c, row0, bh);
+      bulk_commit();
+    }
+  }
 }
 
 }  // namespace fa
