@@ -851,7 +851,9 @@ __device__ __forceinline__ void dq_run(const CUtensorMap& tmQ, const CUtensorMap
 // Each warp step covers RPW consecutive workspace rows (head bh, query q <
 // n_pad), LPR lanes per row, one 16-byte load of O and of dO per lane:
 // -D = -sum_c dO*O and -L * log2(e). Rows q >= n get -D = 0 and -inf, so that
-// recomputed probabilities there are exactly 0.
+// recomputed probabilities there are exactly 0. A warp takes U steps at a time
+// and issues all their loads before any arithmetic (memory-level parallelism:
+// the kernel is bound by reading O and dO from HBM).
 template <int D>
 __global__ void __launch_bounds__(256) preprocess_kernel(const __nv_bfloat16* __restrict__ O,
                                                          const __nv_bfloat16* __restrict__ dO,
@@ -861,29 +863,42 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const __nv_bfloat16* __
                                                          int n_pad, int d, long long rows) {
   constexpr int LPR = D / 8;     // lanes per row (8 bf16 per lane)
   constexpr int RPW = 32 / LPR;  // rows per warp step
+  constexpr int U = 4;           // warp steps in flight
   const int lane = threadIdx.x & 31;
   const int sub = lane % LPR;
   const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
-  for (long long base = ((long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * RPW;
-       base < rows; base += warps * RPW) {
-    const long long r = base + lane / LPR;  // rows is a multiple of RPW (n_pad % 128 == 0)
-    const long long bh = r / n_pad;
-    const int q = (int)(r - bh * n_pad);
-    float acc = 0.f;
-    if (q < n && 8 * sub < d) {
-      const size_t off = ((size_t)bh * n + q) * d;
-      const uint4 a = reinterpret_cast<const uint4*>(O + off)[sub];
-      const uint4 b = reinterpret_cast<const uint4*>(dO + off)[sub];
-      acc = bf16_lo(a.x) * bf16_lo(b.x) + bf16_hi(a.x) * bf16_hi(b.x) +
-            bf16_lo(a.y) * bf16_lo(b.y) + bf16_hi(a.y) * bf16_hi(b.y) +
-            bf16_lo(a.z) * bf16_lo(b.z) + bf16_hi(a.z) * bf16_hi(b.z) +
-            bf16_lo(a.w) * bf16_lo(b.w) + bf16_hi(a.w) * bf16_hi(b.w);
+  for (long long base = ((long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * RPW * U;
+       base < rows; base += warps * RPW * U) {
+    // base is a multiple of RPW * U, which divides n_pad: the U * RPW rows of this
+    // iteration are queries q0 .. q0 + U * RPW - 1 of one head
+    const long long bh = base / n_pad;
+    const int q0 = (int)(base - bh * n_pad) + lane / LPR;
+    const __nv_bfloat16* o_head = O + (size_t)bh * n * d;
+    const __nv_bfloat16* do_head = dO + (size_t)bh * n * d;
+    uint4 a[U], b[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int q = q0 + u * RPW;
+      a[u] = b[u] = make_uint4(0u, 0u, 0u, 0u);  // zero products for rows and lanes past the data
+      if (q < n && 8 * sub < d) {
+        a[u] = reinterpret_cast<const uint4*>(o_head + (size_t)q * d)[sub];
+        b[u] = reinterpret_cast<const uint4*>(do_head + (size_t)q * d)[sub];
+      }
     }
 #pragma unroll
-    for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (sub == 0) {
-      ws_nD[r] = -acc;
-      ws_nL2[r] = (q < n) ? -L[(size_t)bh * n + q] * kLog2e : -INFINITY;
+    for (int u = 0; u < U; ++u) {
+      const int q = q0 + u * RPW;
+      float acc = bf16_lo(a[u].x) * bf16_lo(b[u].x) + bf16_hi(a[u].x) * bf16_hi(b[u].x) +
+                  bf16_lo(a[u].y) * bf16_lo(b[u].y) + bf16_hi(a[u].y) * bf16_hi(b[u].y) +
+                  bf16_lo(a[u].z) * bf16_lo(b[u].z) + bf16_hi(a[u].z) * bf16_hi(b[u].z) +
+                  bf16_lo(a[u].w) * bf16_lo(b[u].w) + bf16_hi(a[u].w) * bf16_hi(b[u].w);
+#pragma unroll
+      for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (sub == 0) {
+        const size_t r = (size_t)bh * n_pad + q;
+        ws_nD[r] = -acc;
+        ws_nL2[r] = (q < n) ? -L[(size_t)bh * n + q] * kLog2e : -INFINITY;
+      }
     }
   }
 }
@@ -1017,19 +1032,20 @@ cudaError_t launch_bwd_d(const BwdArgs& a, bool with_kv, bool with_dq, cudaStrea
   return cudaGetLastError();
 }
 
-int grid_for(long long work_items, int per_block) {
-  long long b = (work_items + per_block - 1) / per_block;
-  const long long cap = 152LL * 16;  // a few waves over the SMs; grid-stride beyond
-  if (b > cap) b = cap;
-  return (int)(b < 1 ? 1 : b);
-}
-
 }  // namespace
 
 cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t s) {
   const long long rows = (long long)a.BH * a.n_pad;
   const bool wide = a.d > 64;
-  const int grid = grid_for(rows / (wide ? 2 : 4), 8);  // warp steps, 8 warps a block
+  // 4 warp steps of 2 (d > 64) or 4 rows per warp, 8 warps a block, at most one
+  // full-occupancy wave (8 blocks of 256 threads per SM); grid-stride beyond.
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long rows_per_block = (wide ? 2 : 4) * 4 * 8;
+  long long blocks = (rows + rows_per_block - 1) / rows_per_block;
+  if (blocks > 8LL * sms) blocks = 8LL * sms;
+  const int grid = (int)(blocks < 1 ? 1 : blocks);
   if (wide)
     preprocess_kernel<128><<<grid, 256, 0, s>>>(
         static_cast<const __nv_bfloat16*>(a.O), static_cast<const __nv_bfloat16*>(a.dO), a.L,
