@@ -201,12 +201,6 @@ struct KvParams {
   float scale, scale_log2;
 };
 
-// Item of round r for CTA c of P in the persistent schedule: rounds alternate their
-// direction so that, with the items in heaviest-first order, every CTA gets about
-// the same total work.
-__device__ __forceinline__ int snake_item(int r, int c, int P) {
-  return r * P + ((r & 1) ? P - 1 - c : c);
-}
 
 // TMEM column of k-step kk (16 queries) of the P^T (part 0) or dS^T (part 1)
 // operand of a half stored in region `reg`.

@@ -13,9 +13,13 @@
 // reference, so the result is the same up to rounding while most blocks need
 // no rescaling of O.
 //
-// GB300 mapping (one CTA per (pair of query tiles, head), 384 threads):
-//   warp 0       TMA producer: both Q tiles (the ring's first slot), then K_j
-//                and V_j (128 keys each) into a ring shared by the two tiles
+// GB300 mapping (one persistent CTA per SM, 384 threads). The work items are
+// (pair of 128-row query tiles, head); CTA c takes items c, 2P - 1 - c, 2P + c, ...
+// of the launch-order list (P CTAs, heaviest items first within a group of heads).
+//   warp 0       TMA producer: per item both Q tiles (one ring slot), then K_j
+//                and V_j (128 keys each) into a ring shared by the two tiles; the
+//                ring runs on across items, so the next item's Q and first blocks
+//                arrive while the current item finishes
 //   warp 1       MMA issuer (whole warp, one elected lane issues). Keys are
 //                taken in steps of 64 (half a loaded block): S_t = Q_t K^T (TS:
 //                Q_t read from TMEM) and O_t += P_t V (TS: P_t read from TMEM),
@@ -26,8 +30,9 @@
 //                tile (= TMEM lane r): reads the 64 S columns of a step with
 //                tcgen05.ld, masks, updates (m, l) in base 2 (exp2 via
 //                ex2.approx), writes P as bf16 over the first 32 of them,
-//                rescales its O row when m moved, and runs the epilogue. While
-//                one tile's softmax runs, the tensor cores work on the other.
+//                rescales its O row when m moved, and runs the epilogue (O_t
+//                leaves TMEM before the next item's Q_t enters). While one tile's
+//                softmax runs, the tensor cores work on the other.
 // TMEM (512 columns at d = 128): Q0, Q1 (d/2 each, bf16 pairs), S0, S1 (64
 // each), O0, O1 (d each). Scores, probabilities and the accumulators never
 // leave the SM.
@@ -119,16 +124,25 @@ __global__ void __launch_bounds__(384, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // Heads a group at a time (their K/V stay in L2 while the group runs); inside
-  // a group the heaviest tile pairs (the last ones, under causal masking) go first.
-  int pair, bh;
-  grouped_tile(blockIdx.x, p.BH, p.num_pairs, p.group, pair, bh);
-  if (p.causal) pair = p.num_pairs - 1 - pair;
-  const int qs = pair * (C::TILES * C::BM);
-  const int nh0 = tile_steps(qs, p.n, p.m, p.causal);
-  const int nh1 = tile_steps(qs + C::BM, p.n, p.m, p.causal);
-  const int nh = max(nh0, nh1);     // 64-key steps of the CTA
-  const int nkb = (nh + 1) / 2;     // 128-key blocks loaded
+  // Persistent: CTA c takes items snake_item(j, c, P), j = 0, 1, ... of the list of
+  // (tile pair, head) items in launch order: heads a group at a time (their K/V
+  // stay in L2 while the group runs), inside a group the heaviest tile pairs (the
+  // last ones, under causal masking) first.
+  const int P = gridDim.x, cta = blockIdx.x;
+  const int n_items = p.num_pairs * p.BH;
+  int n_mine = 0;
+  while (snake_item(n_mine, cta, P) < n_items) ++n_mine;
+  // Item j: first query, head and 64-key steps of each tile (tile 0 always has some).
+  auto item = [&](int j, int& qs, int& bh, int& nh0, int& nh1) {
+    int pair;
+    grouped_tile(snake_item(j, cta, P), p.BH, p.num_pairs, p.group, pair, bh);
+    if (p.causal) pair = p.num_pairs - 1 - pair;
+    qs = pair * (C::TILES * C::BM);
+    nh0 = tile_steps(qs, p.n, p.m, p.causal);
+    nh1 = tile_steps(qs + C::BM, p.n, p.m, p.causal);
+  };
+  // Ring uses of item j: one for its two Q tiles, then one per 128-key block of K, V.
+  // Every role counts them (`ru`) and the steps of each tile identically.
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -156,35 +170,45 @@ __global__ void __launch_bounds__(384, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // Ring use 0: the two Q tiles (slot 0's K and V buffers); use j + 1: K_j, V_j.
-    if (lane == 0 && nh > 0) {
+    // Per item: the two Q tiles into the K and V buffers of one ring slot, then
+    // K_j, V_j per block. The ring runs on across items, so the next item's Q and
+    // first blocks load while the current item finishes.
+    if (lane == 0 && n_mine > 0) {
       tma_prefetch_map(&tmQ);
       tma_prefetch_map(&tmK);
       tma_prefetch_map(&tmV);
-      int issued = 0;
-      for (int u = 0; u <= nkb; ++u) {
-        const int s = u % C::STAGES;
-        if (u >= C::STAGES && !mbar_wait(&bar[C::B_KVE + s], ((u / C::STAGES) & 1) ^ 1, wc))
-          break;
-        uint64_t* f = &bar[C::B_KVF + s];
-        mbar_arrive_expect_tx(f, 2 * C::TILE);
+      int ru = 0;
+      bool ok = true;
+      for (int j = 0; ok && j < n_mine; ++j) {
+        int qs, bh, nh0, nh1;
+        item(j, qs, bh, nh0, nh1);
+        const int nkb = (max(nh0, nh1) + 1) / 2;  // 128-key blocks
+        for (int u = 0; u <= nkb; ++u, ++ru) {
+          const int s = ru % C::STAGES;
+          if (ru >= C::STAGES &&
+              !mbar_wait(&bar[C::B_KVE + s], ((ru / C::STAGES) & 1) ^ 1, wc)) {
+            ok = false;
+            break;
+          }
+          uint64_t* f = &bar[C::B_KVF + s];
+          mbar_arrive_expect_tx(f, 2 * C::TILE);
 #pragma unroll
-        for (int c = 0; c < C::KCH; ++c) {
-          if (u == 0) {
-            tma_load_3d(smem + C::OFF_K + c * C::CHUNK, &tmQ, f, c * 64, qs, bh);
-            tma_load_3d(smem + C::OFF_V + c * C::CHUNK, &tmQ, f, c * 64, qs + C::BM, bh);
-          } else {
-            tma_load_3d(smem + C::OFF_K + s * C::TILE + c * C::CHUNK, &tmK, f, c * 64,
-                        (u - 1) * C::BN, bh);
-            tma_load_3d(smem + C::OFF_V + s * C::TILE + c * C::CHUNK, &tmV, f, c * 64,
-                        (u - 1) * C::BN, bh);
+          for (int c = 0; c < C::KCH; ++c) {
+            uint8_t* kdst = smem + C::OFF_K + s * C::TILE + c * C::CHUNK;
+            uint8_t* vdst = smem + C::OFF_V + s * C::TILE + c * C::CHUNK;
+            if (u == 0) {
+              tma_load_3d(kdst, &tmQ, f, c * 64, qs, bh);
+              tma_load_3d(vdst, &tmQ, f, c * 64, qs + C::BM, bh);
+            } else {
+              tma_load_3d(kdst, &tmK, f, c * 64, (u - 1) * C::BN, bh);
+              tma_load_3d(vdst, &tmV, f, c * 64, (u - 1) * C::BN, bh);
+            }
           }
         }
-        issued = u + 1;
       }
       // Let every copy this thread issued land before the CTA can exit.
-      for (int u = max(0, issued - C::STAGES); u < issued; ++u)
-        drain_wait(&bar[C::B_KVF + u % C::STAGES], (u / C::STAGES) & 1);
+      for (int r = max(0, ru - C::STAGES); r < ru; ++r)
+        drain_wait(&bar[C::B_KVF + r % C::STAGES], (r / C::STAGES) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -192,59 +216,70 @@ __global__ void __launch_bounds__(384, 1)
     //   S_0(0) S_1(0) | O_0 += P_0(0) V, S_0(1), O_1 += P_1(0) V, S_1(1) | ...
     // S_t(k+1) overwrites P_t(k), read by the O_t product issued just before it
     // (tcgen05.mma instructions of one thread execute in order).
-    if (nh > 0) {
+    if (n_mine > 0) {
       constexpr uint32_t kIdescS = idesc_bf16_f32(128, 64, false, false);
       constexpr uint32_t kIdescO = idesc_bf16_f32(128, D, false, true);
-      auto slot_of = [&](int k) { return ((k >> 1) + 1) % C::STAGES; };
-      auto scores = [&](int t, int k) {
-        const uint64_t b_k = sdesc_sw128(
-            smem_u32(smem + C::OFF_K + slot_of(k) * C::TILE + (k & 1) * C::HALF_ROWS), 16, 1024);
+      int ru = 0, base0 = 0, base1 = 0;  // ring uses and steps of earlier items
+      bool ok = true;
+      for (int j = 0; ok && j < n_mine; ++j) {
+        int qs, bh, nh0, nh1;
+        item(j, qs, bh, nh0, nh1);
+        const int nh = max(nh0, nh1), nkb = (nh + 1) / 2;
+        const int nht[2] = {nh0, nh1};
+        const int base[2] = {base0, base1};
+        auto use_of = [&](int k) { return ru + 1 + (k >> 1); };  // ring use of step k's block
+        auto scores = [&](int t, int k) {
+          const uint64_t b_k = sdesc_sw128(
+              smem_u32(smem + C::OFF_K + (use_of(k) % C::STAGES) * C::TILE + (k & 1) * C::HALF_ROWS),
+              16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
-          umma_ts_w(tmem + C::COL_S + 64 * t, tmem + C::COL_Q + (D / 2) * t + kk * 8,
-                    sdesc_add(b_k, off), kIdescS, kk > 0);
-        }
-        umma_commit_w(&bar[C::B_SF + t]);
-      };
-      auto pv = [&](int t, int k) {
-        const uint64_t b_mn = sdesc_sw128(
-            smem_u32(smem + C::OFF_V + slot_of(k) * C::TILE + (k & 1) * C::HALF_ROWS), C::CHUNK,
-            1024);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
+            umma_ts_w(tmem + C::COL_S + 64 * t, tmem + C::COL_Q + (D / 2) * t + kk * 8,
+                      sdesc_add(b_k, off), kIdescS, kk > 0);
+          }
+          umma_commit_w(&bar[C::B_SF + t]);
+        };
+        auto pv = [&](int t, int k) {
+          const uint64_t b_mn = sdesc_sw128(
+              smem_u32(smem + C::OFF_V + (use_of(k) % C::STAGES) * C::TILE + (k & 1) * C::HALF_ROWS),
+              C::CHUNK, 1024);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          umma_ts_w(tmem + C::COL_O + D * t, tmem + C::COL_S + 64 * t + kk * 8,
-                    sdesc_add(b_mn, kk * 2048), kIdescO, (k > 0 || kk > 0) ? 1u : 0u);
-      };
-      const int nht[2] = {nh0, nh1};
-      bool ok = warp_wait(&bar[C::B_IN], 0, wc);
-      if (ok) {
-        if (lane == 0) mbar_arrive(&bar[C::B_KVE + 0]);  // the Q tiles are in TMEM
-        ok = warp_wait(&bar[C::B_KVF + 1 % C::STAGES], (1 / C::STAGES) & 1, wc);
-      }
-      if (ok) {
+          for (int kk = 0; kk < 4; ++kk)
+            umma_ts_w(tmem + C::COL_O + D * t, tmem + C::COL_S + 64 * t + kk * 8,
+                      sdesc_add(b_mn, kk * 2048), kIdescO, (k > 0 || kk > 0) ? 1u : 0u);
+        };
+        // Q_0, Q_1 in TMEM (so the previous item's O_t have been read out too)
+        if (!warp_wait(&bar[C::B_IN], j & 1, wc)) { ok = false; break; }
+        if (lane == 0) mbar_arrive(&bar[C::B_KVE + ru % C::STAGES]);  // the Q slot is free
+        const int u1 = use_of(0);
+        if (!warp_wait(&bar[C::B_KVF + u1 % C::STAGES], (u1 / C::STAGES) & 1, wc)) { ok = false; break; }
         tc_fence_after();
         if (nh0 > 0) scores(0, 0);
         if (nh1 > 0) scores(1, 0);
-      }
-      for (int k = 0; ok && k < nh; ++k) {
-        if (k + 1 < nh && ((k + 1) & 1) == 0) {  // step k+1 opens block (k+1)/2
-          const int u = ((k + 1) >> 1) + 1;
-          if (!warp_wait(&bar[C::B_KVF + u % C::STAGES], (u / C::STAGES) & 1, wc)) break;
-        }
+        for (int k = 0; ok && k < nh; ++k) {
+          if (k + 1 < nh && ((k + 1) & 1) == 0) {  // step k+1 opens block (k+1)/2
+            const int u = use_of(k + 1);
+            if (!warp_wait(&bar[C::B_KVF + u % C::STAGES], (u / C::STAGES) & 1, wc)) { ok = false; break; }
+          }
 #pragma unroll
-        for (int t = 0; t < C::TILES; ++t) {
-          if (k >= nht[t]) continue;
-          if (!warp_wait(&bar[C::B_PF + t], k & 1, wc)) { ok = false; break; }
-          tc_fence_after();
-          pv(t, k);
-          if (k + 1 < nht[t])
-            scores(t, k + 1);
-          else
-            umma_commit_w(&bar[C::B_PVD + t]);
+          for (int t = 0; t < C::TILES; ++t) {
+            if (k >= nht[t]) continue;
+            if (!warp_wait(&bar[C::B_PF + t], (base[t] + k) & 1, wc)) { ok = false; break; }
+            tc_fence_after();
+            pv(t, k);
+            if (k + 1 < nht[t])
+              scores(t, k + 1);
+            else
+              umma_commit_w(&bar[C::B_PVD + t]);
+          }
+          // both tiles are done with block k/2 once its second step is issued
+          if (ok && ((k & 1) || k + 1 == nh))
+            umma_commit_w(&bar[C::B_KVE + use_of(k) % C::STAGES]);
         }
-        // both tiles are done with block k/2 once its second step is issued
-        if (ok && ((k & 1) || k + 1 == nh)) umma_commit_w(&bar[C::B_KVE + slot_of(k)]);
+        ru += 1 + nkb;
+        base0 += nh0;
+        base1 += nh1;
       }
       umma_commit_w(&bar[C::B_DRAIN]);
       drain_wait(&bar[C::B_DRAIN], 0);
@@ -256,125 +291,140 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const uint32_t scol = lane_base + C::COL_S + 64 * t;
     const uint32_t ocol = lane_base + C::COL_O + D * t;
-    const int qg = qs + t * C::BM + row;
-    const int nh_t = t == 0 ? nh0 : nh1;
     const float sl2 = p.scale_log2;
-    float m_ref = -INFINITY;  // reference maximum of S * scale * log2(e)
-    float l_run = 0.f;        // sum of exp2(S * scale * log2(e) - m_ref)
-    bool ok = nh == 0 || warp_wait(&bar[C::B_KVF], 0, wc);
-    if (ok && nh > 0) {
-      // Row `row` of Q_t into TMEM: the row's 16-byte pieces in the 128-byte-
-      // swizzled tile (piece j of a chunk row at j ^ (row % 8)).
-      const uint8_t* tile = smem + (t == 0 ? C::OFF_K : C::OFF_V);
+    int ru = 0, base_t = 0, pvd_t = 0;  // ring uses, steps and finished items of tile t
+    bool ok = true;
+    for (int j = 0; ok && j < n_mine; ++j) {
+      int qs, bh, nh0, nh1;
+      item(j, qs, bh, nh0, nh1);
+      const int nkb = (max(nh0, nh1) + 1) / 2;
+      const int nh_t = t == 0 ? nh0 : nh1;
+      const int qg = qs + t * C::BM + row;
+      float m_ref = -INFINITY;  // reference maximum of S * scale * log2(e)
+      float l_run = 0.f;        // sum of exp2(S * scale * log2(e) - m_ref)
+      // Row `row` of Q_t into TMEM: the row's 16-byte pieces in the 128-byte-swizzled
+      // tile (piece j of a chunk row at j ^ (row % 8)). The previous item's S_t
+      // products, the only readers of these columns, are complete: this warp waited
+      // for each of them.
+      {
+        const int s = ru % C::STAGES;
+        if (!warp_wait(&bar[C::B_KVF + s], (ru / C::STAGES) & 1, wc)) { ok = false; break; }
+        const uint8_t* tile = smem + (t == 0 ? C::OFF_K : C::OFF_V) + s * C::TILE;
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        uint32_t v[32];
-        const uint8_t* src = tile + c * C::CHUNK + row * 128;
+        for (int c = 0; c < D / 64; ++c) {
+          uint32_t v[32];
+          const uint8_t* src = tile + c * C::CHUNK + row * 128;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint4 x = *reinterpret_cast<const uint4*>(src + ((j ^ (row & 7)) << 4));
-          v[4 * j] = x.x;
-          v[4 * j + 1] = x.y;
-          v[4 * j + 2] = x.z;
-          v[4 * j + 3] = x.w;
+          for (int q = 0; q < 8; ++q) {
+            const uint4 x = *reinterpret_cast<const uint4*>(src + ((q ^ (row & 7)) << 4));
+            v[4 * q] = x.x;
+            v[4 * q + 1] = x.y;
+            v[4 * q + 2] = x.z;
+            v[4 * q + 3] = x.w;
+          }
+          tmem_st32(lane_base + C::COL_Q + (D / 2) * t + 32 * c, v);
         }
-        tmem_st32(lane_base + C::COL_Q + (D / 2) * t + 32 * c, v);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bar[C::B_IN]);
       }
-      tmem_st_wait();
-      tc_fence_before();
-    }
-    if (nh > 0) mbar_arrive(&bar[C::B_IN]);
-    for (int k = 0; ok && k < nh_t; ++k) {
-      if (!warp_wait(&bar[C::B_SF + t], k & 1, wc)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t sr[64];
-      tmem_ld32(scol, sr);
-      tmem_ld32(scol + 32, sr + 32);
-      tmem_ld_wait();
-      reg_fence32(sr);
-      reg_fence32(sr + 32);
-
-      // Last visible column of this step for this row (ragged m, causal k <= q).
-      const int ks = 64 * k;
-      int lim = p.m - 1 - ks;
-      if (p.causal) lim = min(lim, qg - ks);
-      if (lim < 63) {
-#pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (c > lim) sr[c] = __float_as_uint(-INFINITY);
-      }
-      // Row maximum: eight chains of three-input maxima.
-      float mx[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) mx[e] = __uint_as_float(sr[e]);
-#pragma unroll
-      for (int c = 8; c < 64; c += 16)
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          mx[e] = max3f(mx[e], __uint_as_float(sr[c + e]), __uint_as_float(sr[c + 8 + e]));
-      const float rmax = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]),
-                               fmaxf(mx[6], mx[7])) * sl2;
-      // Move the reference only when the row maximum passed it by the threshold.
-      const bool move = rmax > m_ref + kRescaleThreshold;
-      const float m_new = move ? rmax : m_ref;
-      const float corr = move ? ex2(m_ref - m_new) : 1.f;  // 0 on the first step
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;  // no (-inf) - (-inf)
-      m_ref = m_new;
-      // P = exp2(S * scale * log2(e) - m) as bf16 pairs over this row's own S
-      // columns.
-      const uint64_t sl2x2 = f2pack(sl2, sl2);
-      const uint64_t negm2 = f2pack(-m_use, -m_use);
-      uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
-      uint32_t pp[32];
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const uint64_t x2 = ffma2(
-            f2pack(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), sl2x2, negm2);
-        float x0, x1;
-        f2unpack(x2, x0, x1);
-        const float p0 = ex2(x0), p1 = ex2(x1);
-        acc2[c & 3] = fadd2(acc2[c & 3], f2pack(p0, p1));
-        pp[c] = pack_bf16(p0, p1);
-      }
-      // S_t(k) completing implies O_t += P_t(k-1) V completed (issued before it),
-      // so the O row may be rescaled before this step's product is signalled.
-      if (k >= 1 && __any_sync(0xffffffffu, move)) {
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(ocol + 32 * c, o);
-          tmem_ld_wait();
-          reg_fence32(o);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
-          tmem_st32(ocol + 32 * c, o);
+      for (int k = 0; ok && k < nh_t; ++k) {
+        if (!warp_wait(&bar[C::B_SF + t], (base_t + k) & 1, wc)) {
+          ok = false;
+          break;
         }
-      }
-      tmem_st32(scol, pp);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&bar[C::B_PF + t]);
-      float s0, s1, s2, s3, s4, s5, s6, s7;
-      f2unpack(acc2[0], s0, s1);
-      f2unpack(acc2[1], s2, s3);
-      f2unpack(acc2[2], s4, s5);
-      f2unpack(acc2[3], s6, s7);
-      l_run = l_run * corr + (((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7)));
-    }
+        tc_fence_after();
+        uint32_t sr[64];
+        tmem_ld32(scol, sr);
+        tmem_ld32(scol + 32, sr + 32);
+        tmem_ld_wait();
+        reg_fence32(sr);
+        reg_fence32(sr + 32);
 
-    // ------------------------------------------------------------ epilogue
-    if (ok && nh_t > 0 && warp_wait(&bar[C::B_PVD + t], 0, wc)) {
-      tc_fence_after();
-      // O / l as bf16 through the warp's staging area and TMA (rows past n and the
-      // zero columns past d are not written)
-      tmem_rows_store<D>(ocol, 1.f / l_run, smem + C::OFF_EPI + (warp - 4) * kStoreStageBytes,
-                         &tmO, 0, qs + t * C::BM + ((warp - 4) & 3) * 32, p.n, bh, p.d);
-      if (qg < p.n) p.L[(size_t)bh * p.n + qg] = (m_ref + lg2(l_run)) * kLn2;
-      if (lane == 0) bulk_wait_all();  // the stores have read the staging buffers
+        // Last visible column of this step for this row (ragged m, causal k <= q).
+        const int ks = 64 * k;
+        int lim = p.m - 1 - ks;
+        if (p.causal) lim = min(lim, qg - ks);
+        if (lim < 63) {
+  #pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (c > lim) sr[c] = __float_as_uint(-INFINITY);
+        }
+        // Row maximum: eight chains of three-input maxima.
+        float mx[8];
+  #pragma unroll
+        for (int e = 0; e < 8; ++e) mx[e] = __uint_as_float(sr[e]);
+  #pragma unroll
+        for (int c = 8; c < 64; c += 16)
+  #pragma unroll
+          for (int e = 0; e < 8; ++e)
+            mx[e] = max3f(mx[e], __uint_as_float(sr[c + e]), __uint_as_float(sr[c + 8 + e]));
+        const float rmax = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]),
+                                 fmaxf(mx[6], mx[7])) * sl2;
+        // Move the reference only when the row maximum passed it by the threshold.
+        const bool move = rmax > m_ref + kRescaleThreshold;
+        const float m_new = move ? rmax : m_ref;
+        const float corr = move ? ex2(m_ref - m_new) : 1.f;  // 0 on the first step
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;  // no (-inf) - (-inf)
+        m_ref = m_new;
+        // P = exp2(S * scale * log2(e) - m) as bf16 pairs over this row's own S
+        // columns.
+        const uint64_t sl2x2 = f2pack(sl2, sl2);
+        const uint64_t negm2 = f2pack(-m_use, -m_use);
+        uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+        uint32_t pp[32];
+  #pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const uint64_t x2 = ffma2(
+              f2pack(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), sl2x2, negm2);
+          float x0, x1;
+          f2unpack(x2, x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          acc2[c & 3] = fadd2(acc2[c & 3], f2pack(p0, p1));
+          pp[c] = pack_bf16(p0, p1);
+        }
+        // S_t(k) completing implies O_t += P_t(k-1) V completed (issued before it),
+        // so the O row may be rescaled before this step's product is signalled.
+        if (k >= 1 && __any_sync(0xffffffffu, move)) {
+  #pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(ocol + 32 * c, o);
+            tmem_ld_wait();
+            reg_fence32(o);
+  #pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
+            tmem_st32(ocol + 32 * c, o);
+          }
+        }
+        tmem_st32(scol, pp);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bar[C::B_PF + t]);
+        float s0, s1, s2, s3, s4, s5, s6, s7;
+        f2unpack(acc2[0], s0, s1);
+        f2unpack(acc2[1], s2, s3);
+        f2unpack(acc2[2], s4, s5);
+        f2unpack(acc2[3], s6, s7);
+        l_run = l_run * corr + (((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7)));
+      }
+
+      // ---------------------------------------------------------- epilogue
+      if (ok && nh_t > 0) {
+        if (!warp_wait(&bar[C::B_PVD + t], pvd_t & 1, wc)) { ok = false; break; }
+        tc_fence_after();
+        // O / l as bf16 through the warp's staging area and TMA (rows past n and
+        // the zero columns past d are not written)
+        tmem_rows_store<D>(ocol, 1.f / l_run, smem + C::OFF_EPI + (warp - 4) * kStoreStageBytes,
+                           &tmO, 0, qs + t * C::BM + ((warp - 4) & 3) * 32, p.n, bh, p.d);
+        if (qg < p.n) p.L[(size_t)bh * p.n + qg] = (m_ref + lg2(l_run)) * kLn2;
+        tc_fence_before();  // O_t read out before the next item's products overwrite it
+        ++pvd_t;
+      }
+      ru += 1 + nkb;
+      base_t += nh_t;
     }
+    if (lane == 0) bulk_wait_all();  // the stores have read the staging buffers
   }
 
   tc_fence_before();
@@ -409,7 +459,12 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
   cudaError_t e =
       cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  const unsigned grid = (unsigned)p.num_pairs * (unsigned)a.BH;
+  // One CTA per SM (persistent), fewer when there are fewer items.
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long items = (long long)p.num_pairs * a.BH;
+  const unsigned grid = (unsigned)(items < sms ? items : sms);
   fwd_kernel<D><<<grid, C::THREADS, C::SMEM, stream>>>(mq, mk, mv, mo, p);
   return cudaGetLastError();
 }

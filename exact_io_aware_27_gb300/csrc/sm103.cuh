@@ -102,6 +102,11 @@ FA_DEV void grouped_tile(int lin, int BH, int tiles, int group, int& rank, int& 
   bh = base + r % gsize;
 }
 
+// Item of round r for CTA c of P in a persistent schedule: rounds alternate their
+// direction so that, with the items in heaviest-first order, every CTA gets about
+// the same total work.
+FA_DEV int snake_item(int r, int c, int P) { return r * P + ((r & 1) ? P - 1 - c : c); }
+
 // ---------------------------------------------------------------- TMA
 FA_DEV void tma_prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
