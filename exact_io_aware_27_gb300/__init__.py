@@ -5,7 +5,7 @@ The compute lives in ``libfa_gb300.so`` (hand-written CUDA, C-ABI in
 load the library; the first call does, and raises if it has not been built.
 """
 from ._build import build  # noqa: F401
-from .api import (FAError, FlashAttention, alloc_workspace, fa_backward,  # noqa: F401
+from .api import (FAError, FlashAttention, Session, alloc_workspace, fa_backward,  # noqa: F401
                   fa_backward_dkdv, fa_backward_dq, fa_backward_grads, fa_backward_noalloc,
                   fa_backward_preprocess,
                   fa_backward_workspace_size, fa_forward, fa_get_device_status,

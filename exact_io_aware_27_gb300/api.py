@@ -47,6 +47,9 @@ SIGNATURES = {
     "fa_backward_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P,
                                  _P, _P]),
     "fa_online_softmax_stats": (_I, [_P, ctypes.c_longlong, ctypes.c_longlong, _P, _P, _P]),
+    "fa_session_create": (_I, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_P)]),
+    "fa_session_destroy": (None, [_P]),
+    "fa_session_step": (_I, [_P, _P, _P, _P, _P, _I, _F, _P, _P, _P, _P, _P]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_get_device_status": (_I, [ctypes.POINTER(_I)]),
     "fa_version": (_I, []),
@@ -253,6 +256,53 @@ def fa_online_softmax_stats(x: torch.Tensor, m=None, l=None, stream=None):
                                        _stream(x, stream))
     _check("fa_online_softmax_stats", rc)
     return m, l
+
+
+class Session:
+    """A host-buffer session (fa_session_create / fa_session_step / destroy): one
+    forward + backward step on CPU tensors, pipelined on the GPU over chunks of
+    `chunk_heads` heads. Inputs and outputs are CPU tensors (page-locked ones let
+    the copies run asynchronously); the device is the current CUDA device."""
+
+    def __init__(self, B: int, H: int, n: int, m: int, d: int, chunk_heads: int):
+        self.shape = (B, H, n, m, d)
+        handle = ctypes.c_void_p()
+        _check("fa_session_create",
+               lib().fa_session_create(B, H, n, m, d, chunk_heads, ctypes.byref(handle)))
+        self._handle = handle
+
+    def step(self, Q, K, V, dO, causal: bool = False, scale: float | None = None, O=None,
+             L=None, dQ=None, dK=None, dV=None):
+        """O, L, dQ, dK, dV (CPU tensors, allocated here when not given)."""
+        B, H, n, m, d = self.shape
+        for name, t, rows in (("Q", Q, n), ("K", K, m), ("V", V, m), ("dO", dO, n)):
+            if (t.is_cuda or t.dtype != torch.bfloat16 or tuple(t.shape) != (B, H, rows, d)
+                    or not t.is_contiguous()):
+                raise ValueError(f"{name} must be a contiguous bf16 CPU tensor {(B, H, rows, d)}")
+        pin = Q.is_pinned()
+        new = (lambda like: torch.empty_like(like, pin_memory=pin))
+        O = new(Q) if O is None else O
+        L = torch.empty((B, H, n), dtype=torch.float32, pin_memory=pin) if L is None else L
+        dQ = new(Q) if dQ is None else dQ
+        dK = new(K) if dK is None else dK
+        dV = new(V) if dV is None else dV
+        rc = lib().fa_session_step(self._handle, Q.data_ptr(), K.data_ptr(), V.data_ptr(),
+                                   dO.data_ptr(), int(bool(causal)), _scale(scale, d),
+                                   O.data_ptr(), L.data_ptr(), dQ.data_ptr(), dK.data_ptr(),
+                                   dV.data_ptr())
+        _check("fa_session_step", rc)
+        return O, L, dQ, dK, dV
+
+    def close(self):
+        if self._handle:
+            lib().fa_session_destroy(self._handle)
+            self._handle = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def fa_get_device_status() -> int:

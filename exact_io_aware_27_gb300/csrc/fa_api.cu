@@ -156,6 +156,8 @@ int prepare_backward(const void* Q, const void* K, const void* V, const void* O,
 
 }  // namespace
 
+int validate_sizes(int B, int H, int n, int m, int d) { return check_sizes(B, H, n, m, d); }
+
 int heads_per_group(int BH, int tiles_per_head) {
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess)

@@ -22,6 +22,9 @@ inline int ceil_div(int x, int a) { return (x + a - 1) / a; }
 // earlier (a shorter tail). Eight waves measured best on GB300 for both kernels.
 int heads_per_group(int BH, int tiles_per_head);
 
+// The size rules every entry point applies (FA_OK or the fa_status they return).
+int validate_sizes(int B, int H, int n, int m, int d);
+
 // cuTensorMapEncodeTiled, fetched from the driver at first use.
 CUresult encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, cuuint32_t rank,
                            void* base, const cuuint64_t* dims, const cuuint64_t* strides_bytes,

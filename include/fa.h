@@ -180,6 +180,42 @@ FA_API int fa_backward_noalloc(const void* Q, const void* K, const void* V, cons
 FA_API int fa_online_softmax_stats(const float* x, long long rows, long long cols, float* m,
                                    float* l, void* stream);
 
+/*
+ * Host-buffer sessions: one forward + backward step whose inputs and outputs are
+ * in host memory, for callers that keep their tensors on the host. A session owns
+ * device buffers for `chunk_heads` heads at a time (three sets), a backward
+ * workspace for one chunk and three CUDA streams (copies in, kernels, copies out)
+ * on the device current when it is created.
+ *
+ * fa_session_step splits the B*H heads into chunks of chunk_heads (the last one
+ * may be smaller); for each chunk it copies Q, K, V, dO in, runs fa_forward and
+ * fa_backward on it, and copies O, L, dQ, dK, dV out, so that the copies of one
+ * chunk overlap the kernels of its neighbours and both copy directions run at
+ * once. Results equal those of fa_forward + fa_backward on the whole batch (the
+ * heads are independent). It returns once every output is in host memory. Host
+ * buffers should be page-locked (cudaHostAlloc / cudaHostRegister) for the copies
+ * to run asynchronously; pageable buffers work but serialise.
+ *
+ * fa_session_create: shapes and rules as fa_forward, 1 <= chunk_heads <= B*H.
+ * It allocates device memory (the only entry point that does): three sets of
+ * chunk_heads x (4 n d + 4 m d) bf16 values and chunk_heads x n fp32, plus one
+ * workspace. Returns FA_OK and *out, or a negative fa_status (FA_ERR_CUDA if an
+ * allocation fails; nothing is left allocated then).
+ * fa_session_destroy: waits for the session's streams and frees everything;
+ * NULL is a no-op.
+ * fa_session_step: host pointers; inputs Q, dO [B,H,n,d] and K, V [B,H,m,d]
+ * bf16; outputs O, dQ [B,H,n,d], dK, dV [B,H,m,d] bf16 and L [B,H,n] fp32. Scale
+ * rules as fa_forward. The session's device must be current. Returns FA_OK or
+ * the first error; kernel timeouts are reported by fa_get_device_status().
+ */
+typedef struct fa_session fa_session;
+FA_API int fa_session_create(int B, int H, int n, int m, int d, int chunk_heads,
+                             fa_session** out);
+FA_API void fa_session_destroy(fa_session* s);
+FA_API int fa_session_step(fa_session* s, const void* Q, const void* K, const void* V,
+                           const void* dO, int causal, float scale, void* O, float* L,
+                           void* dQ, void* dK, void* dV);
+
 /* A static, human-readable name for a status code. Never NULL. */
 FA_API const char* fa_status_string(int status);
 
@@ -187,8 +223,9 @@ FA_API const char* fa_status_string(int status);
  * Reads the device status word of the current device into *status_out
  * (FA_OK; FA_ERR_DEVICE_TIMEOUT if a kernel gave up waiting since the last
  * read; FA_ERR_UNSUPPORTED_DEVICE if a kernel found its shared memory placed
- * other than on a 1024-byte boundary and returned without work) and clears it. Synchronises with the device. Returns FA_OK or
- * FA_ERR_CUDA / FA_ERR_INVALID_ARG.
+ * other than on a 1024-byte boundary and returned without work) and clears it.
+ * Synchronises with the device. Returns FA_OK or FA_ERR_CUDA /
+ * FA_ERR_INVALID_ARG.
  */
 FA_API int fa_get_device_status(int* status_out);
 

@@ -145,3 +145,17 @@ def test_online_softmax_argument_errors(lib):
     assert f(x + 2, 4, 8, m, l, None) == api.FA_ERR_MISALIGNED
     assert f(x, 4, 8, x + 16, l, None) == api.FA_ERR_INVALID_ARG  # m inside x
     assert f(x, 4, 8, m, m + 8, None) == api.FA_ERR_INVALID_ARG   # l overlaps m
+
+
+def test_session_argument_errors(lib):
+    import ctypes
+    h = ctypes.c_void_p()
+    assert lib.fa_session_create(1, 1, 8, 8, 64, 1, None) == api.FA_ERR_INVALID_ARG
+    assert lib.fa_session_create(0, 1, 8, 8, 64, 1, ctypes.byref(h)) == api.FA_ERR_INVALID_ARG
+    assert lib.fa_session_create(1, 1, 8, 8, 20, 1, ctypes.byref(h)) == api.FA_ERR_UNSUPPORTED_HEAD_DIM
+    assert lib.fa_session_create(1, 2, 8, 8, 64, 0, ctypes.byref(h)) == api.FA_ERR_INVALID_ARG
+    assert lib.fa_session_create(1, 2, 8, 8, 64, 3, ctypes.byref(h)) == api.FA_ERR_INVALID_ARG
+    assert not h.value  # nothing handed out on failure
+    lib.fa_session_destroy(None)  # a no-op
+    assert lib.fa_session_step(None, FAKE, FAKE, FAKE, FAKE, 0, 0.125, FAKE, FAKE, FAKE, FAKE,
+                               FAKE) == api.FA_ERR_INVALID_ARG
