@@ -5,19 +5,30 @@
 //   dK = dS^T Q * scale; blocks wholly above the diagonal are skipped under
 //   causal masking.
 //
-// Three kernels on one stream:
+// Two kernels on one stream:
 //   preprocess  -D and -L * log2(e) (-inf past n) into the workspace; memory bound.
-//   dkdv        one CTA per (key block of 128, head), looping over query blocks
-//               of 128. The key block's K and V stay in shared memory; dK and dV
-//               accumulate in TMEM and are written once. The transposed
-//               products put the key index on the TMEM lane:
-//                 S^T  = K Q_i^T       dP^T = V dO_i^T     (SS MMAs)
-//                 dV  += P^T dO_i      dK  += dS^T Q_i     (TS MMAs: P^T and dS^T
-//                                                           are written to TMEM)
-//   dq          one CTA per (query block of 128, head), looping over key blocks
-//               of 128, with Q and dO held in TMEM:
-//                 S = Q K_j^T, dP = dO V_j^T, dQ += dS K_j  (TS MMAs)
+//   bwd_kernel  the gradients, persistent: one CTA per SM runs its share of the
+//               dK/dV pass (blocks = (128-key block, head)) and then of the dQ pass
+//               (blocks = (128-query block, head)); the blocks are dealt in
+//               snake order over lists that put the heaviest blocks first within
+//               a group of heads.
+//   dK/dV pass  K is moved into TMEM (the A operand of S^T); V stays in shared
+//               memory (two buffers); Q, dO, -L2 and -D of 64 queries at a time
+//               stream through a ring of half-block slots, which also carries the
+//               next block's K. Per 64-query half u (key index on the TMEM lane):
+//                 S^T = K Q_u^T (TS)       dP^T = V dO_u^T (SS)
+//                 dV += P^T dO_u (TS)      dK  += dS^T Q_u (TS)
+//               with P^T and dS^T written by the compute warps as bf16 over the
+//               S^T columns they have read; S^T alternates between two TMEM regions
+//               so S^T of half u+2 forms while half u is processed. dK and dV
+//               accumulate in TMEM and are written once per block.
+//   dQ pass     Q and dO are moved into TMEM (A operands of S and dP); K and V
+//               stream through a ring. Each 128-key block is taken in halves of 64
+//               keys, one per compute group (ping-pong):
+//                 S_h = Q K_h^T, dP_h = dO V_h^T, dQ += dS_h K_h   (TS)
 //               dQ accumulates in TMEM and is written once, scaled, as bf16.
+//   Epilogues leave TMEM through per-warp swizzled staging in shared memory and
+//   one TMA store per 32 x 32 piece, while the next block's first products run.
 //
 // The pages' loop adds each block's dS K into dQ in memory from inside the key
 // loop. Here dQ is its own pass that recomputes S and dP for its query block:
@@ -28,12 +39,9 @@
 // that have room for it, needs no zeroed accumulator or conversion pass, and
 // makes dQ deterministic.
 //
-// Roles (384 threads in both kernels): warp 0 TMA producer, warp 1 MMA issuer
-// (whole warp, one elected lane issues), warps 4..11 two compute warpgroups,
-// each owning half (64) of the columns of a 128 x 128 score block; thread =
-// TMEM lane (key row in dkdv, query row in dq). The products of each half are
-// formed separately (N = 64) and the two halves are interleaved, so that one
-// group computes probabilities while the tensor cores work for the other.
+// Roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer (whole warp, one
+// elected lane issues), warps 4..11 two compute warpgroups; thread = TMEM lane
+// (key row in the dK/dV pass, query row in the dQ pass).
 #include "fa_internal.h"
 #include "sm103.cuh"
 
