@@ -112,8 +112,9 @@ FA_API int fa_backward(const void* Q, const void* K, const void* V, const void* 
  *   into dQ from inside the key loop; this computes the same sum as its own
  *   pass, with no read-modify-write of dQ in memory).
  * fa_backward_grads: fa_backward_dkdv and fa_backward_dq as one kernel launch
- *   (their thread blocks interleaved); what fa_backward queues after the
- *   preprocess stage. Results are bitwise identical to the two separate calls.
+ *   (persistent: each thread block runs its share of the dK/dV blocks, then of
+ *   the dQ blocks); what fa_backward queues after the preprocess stage. Results
+ *   are bitwise identical to the two separate calls.
  */
 FA_API int fa_backward_preprocess(const void* O, const void* dO, const float* L, int B, int H, int n,
                            int d, void* workspace, size_t workspace_bytes, void* stream);
