@@ -63,7 +63,7 @@ cudaError_t launch_forward(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t s);
-// dK, dV and dQ in one launch (the two passes' CTAs interleaved).
+// dK, dV and dQ in one persistent launch (each CTA: its dK/dV blocks, then its dQ blocks).
 cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t s);
 
 // Online softmax statistics of fp32 rows (m, l per row).
