@@ -1,8 +1,9 @@
 // Host-buffer sessions (see include/fa.h): one forward + backward step whose
 // inputs and outputs live in host memory, pipelined over chunks of heads.
 //
-// Heads are independent in both passes, so a step splits B*H into chunks of
-// `chunk_heads` heads and runs three streams: copies in (Q, K, V, dO of chunk c),
+// Heads are independent in both passes, so a step splits B*H into chunks of at
+// most `chunk_heads` heads (the first and the last of half that size, which
+// shortens the pipeline's fill and drain) and runs three streams: copies in (Q, K, V, dO of chunk c),
 // kernels (fa_forward then fa_backward on chunk c) and copies out (O, L, dQ, dK,
 // dV of chunk c). Chunk c uses buffer set c % 3; events order each stage after
 // the previous stage of its chunk and the copies in of chunk c + 3 after the
@@ -15,12 +16,17 @@
 #include "fa.h"
 #include "fa_internal.h"
 
+namespace fa {
+constexpr int kSessionSets = 3;  // buffer sets: chunk c uses set c % kSessionSets
+}  // namespace fa
+
 struct fa_session {
   int B, H, n, m, d, chunk, device;
   cudaStream_t in, comp, out;
-  cudaEvent_t ev_in[3], ev_comp[3], ev_out[3];
-  void *Q[3], *K[3], *V[3], *dO[3], *O[3], *dQ[3], *dK[3], *dV[3];
-  float* L[3];
+  cudaEvent_t ev_in[fa::kSessionSets], ev_comp[fa::kSessionSets], ev_out[fa::kSessionSets];
+  void *Q[fa::kSessionSets], *K[fa::kSessionSets], *V[fa::kSessionSets], *dO[fa::kSessionSets];
+  void *O[fa::kSessionSets], *dQ[fa::kSessionSets], *dK[fa::kSessionSets], *dV[fa::kSessionSets];
+  float* L[fa::kSessionSets];
   void* ws;
   size_t ws_bytes;
 };
@@ -28,7 +34,7 @@ struct fa_session {
 namespace fa {
 namespace {
 
-constexpr int kSets = 3;
+constexpr int kSets = kSessionSets;
 
 void release(fa_session* s) {
   if (!s) return;
@@ -121,7 +127,9 @@ int fa_session_step(fa_session* s, const void* Q, const void* K, const void* V, 
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
   if (dev != s->device) return FA_ERR_INVALID_ARG;
   const int BH = s->B * s->H, n = s->n, m = s->m, d = s->d;
-  const int chunks = (BH + s->chunk - 1) / s->chunk;
+  // chunk sizes: half, full, ..., full, then the rest as two halves when it is a
+  // full chunk (all at most s->chunk heads)
+  const int half = (s->chunk + 1) / 2;
   const auto* hq = static_cast<const uint8_t*>(Q);
   const auto* hk = static_cast<const uint8_t*>(K);
   const auto* hv = static_cast<const uint8_t*>(V);
@@ -131,9 +139,12 @@ int fa_session_step(fa_session* s, const void* Q, const void* K, const void* V, 
   auto* hdk = static_cast<uint8_t*>(dK);
   auto* hdv = static_cast<uint8_t*>(dV);
   int rc = FA_OK;
-  for (int c = 0; rc == FA_OK && c < chunks; ++c) {
+  for (int c = 0, h0 = 0; rc == FA_OK && h0 < BH; ++c) {
     const int i = c % kSets;
-    const int h0 = c * s->chunk, hc = (BH - h0 < s->chunk) ? BH - h0 : s->chunk;
+    const int left = BH - h0;
+    int hc = c == 0 ? half : s->chunk;
+    if (left <= s->chunk) hc = (left > half && c > 0) ? left - half : left;  // end with a half chunk
+    if (hc > left) hc = left;
     const size_t qoff = (size_t)h0 * n * d * 2, koff = (size_t)h0 * m * d * 2;
     const size_t qn = (size_t)hc * n * d * 2, km = (size_t)hc * m * d * 2;
     // copies in, once the copies out of the chunk that last used this set are done
@@ -162,6 +173,7 @@ int fa_session_step(fa_session* s, const void* Q, const void* K, const void* V, 
     if (rc == FA_OK) rc = copy_out(hdk + koff, s->dK[i], km, s->out);
     if (rc == FA_OK) rc = copy_out(hdv + koff, s->dV[i], km, s->out);
     if (rc == FA_OK && cudaEventRecord(s->ev_out[i], s->out) != cudaSuccess) rc = FA_ERR_CUDA;
+    h0 += hc;
   }
   // whatever was queued finishes before the call returns (the host buffers are the caller's)
   const bool synced = cudaStreamSynchronize(s->in) == cudaSuccess &&
