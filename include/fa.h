@@ -188,8 +188,9 @@ FA_API int fa_online_softmax_stats(const float* x, long long rows, long long col
  * workspace for one chunk and three CUDA streams (copies in, kernels, copies out)
  * on the device current when it is created.
  *
- * fa_session_step splits the B*H heads into chunks of chunk_heads (the last one
- * may be smaller); for each chunk it copies Q, K, V, dO in, runs fa_forward and
+ * fa_session_step splits the B*H heads into chunks of at most chunk_heads (the
+ * first and the last of about half that size, which shortens the pipeline's fill
+ * and drain); for each chunk it copies Q, K, V, dO in, runs fa_forward and
  * fa_backward on it, and copies O, L, dQ, dK, dV out, so that the copies of one
  * chunk overlap the kernels of its neighbours and both copy directions run at
  * once. Results equal those of fa_forward + fa_backward on the whole batch (the
