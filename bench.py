@@ -342,7 +342,8 @@ def run_ours(args):
     if not args.no_e2e:
         # End to end through the C-ABI host-buffer call (fa_session_step): pinned
         # host inputs in, forward + backward, every output back in host memory, each
-        # step; the session pipelines the copies and kernels over 8 chunks of heads.
+        # step; the session pipelines the copies and kernels over chunks of at most
+        # B*H/8 heads.
         hq, hk, hv, hdo = (t.pin_memory() for t in (Q, K, V, dO))
         ho, hl = torch.empty_like(hq).pin_memory(), torch.empty((B, H, n), dtype=torch.float32).pin_memory()
         hdq, hdk, hdv = (torch.empty_like(t).pin_memory() for t in (hq, hk, hv))
@@ -369,7 +370,7 @@ def run_ours(args):
         e2e_value = weak_value(flops_step, world, e2e_ms)
         e2e = {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-               "api": f"fa_session_step, host buffers, {-(-(B * H) // chunk)} chunks of {chunk} heads"}
+               "api": f"fa_session_step, host buffers, chunks of at most {chunk} heads"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
