@@ -269,9 +269,10 @@ def test_autograd_squared_output_loss(causal):
         assert err <= parity.GRAD_REL, f"{name} relative Frobenius error {err:.3e}"
 
 
-def test_stage_entry_points_match_fa_backward():
-    B, H, n, m, d = 1, 2, 300, 300, 128
-    Q, K, V, dO = (t.cuda() for t in wl.attention_inputs(B, H, n, m, d, seed=7800))
+@pytest.mark.parametrize("d", [128, 64, 40])
+def test_stage_entry_points_match_fa_backward(d):
+    B, H, n, m = 1, 2, 300, 300
+    Q, K, V, dO = (t.cuda() for t in wl.attention_inputs(B, H, n, m, d, seed=7800 + d))
     O, L = fa.fa_forward(Q, K, V, True)
     dQ, dK, dV = fa.fa_backward(Q, K, V, O, L, dO, True)
     ws = fa.alloc_workspace(B, H, n, m, d, Q.device)
