@@ -296,3 +296,37 @@ def test_repeatable_and_no_timeout():
     for a, b in zip(r1, r2):  # no atomics anywhere: identical bits
         assert torch.equal(a, b)
     assert fa.fa_get_device_status() == 0
+
+
+@pytest.mark.parametrize("d,causal", [(128, True), (64, False)])
+def test_cuda_graph_capture_and_replay(d, causal):
+    """The C-ABI calls are stream-ordered and allocation-free given their buffers, so a
+    forward + backward step can be captured in a CUDA graph; replays equal eager calls."""
+    B, H, n, m = 1, 3, 333, 333
+    Q, K, V, dO = (t.cuda() for t in wl.attention_inputs(B, H, n, m, d, seed=8500 + d))
+    O, L = fa.fa_forward(Q, K, V, causal)
+    dQ, dK, dV = fa.fa_backward(Q, K, V, O, L, dO, causal)
+    torch.cuda.synchronize()
+    ref = [t.clone() for t in (O, L, dQ, dK, dV)]
+    gO, gL = torch.empty_like(O), torch.empty_like(L)
+    gdQ, gdK, gdV = torch.empty_like(dQ), torch.empty_like(dK), torch.empty_like(dV)
+    ws = fa.alloc_workspace(B, H, n, m, d, Q.device)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # warm-up on the capture stream
+        fa.fa_forward(Q, K, V, causal, O=gO, L=gL)
+        fa.fa_backward(Q, K, V, gO, gL, dO, causal, dQ=gdQ, dK=gdK, dV=gdV, workspace=ws)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    for t in (gO, gL, gdQ, gdK, gdV):
+        t.zero_()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        fa.fa_forward(Q, K, V, causal, O=gO, L=gL)
+        fa.fa_backward(Q, K, V, gO, gL, dO, causal, dQ=gdQ, dK=gdK, dV=gdV, workspace=ws)
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    for name, a, b in zip(("O", "L", "dQ", "dK", "dV"), (gO, gL, gdQ, gdK, gdV), ref):
+        assert torch.equal(a, b), name
+    assert fa.fa_get_device_status() == 0
