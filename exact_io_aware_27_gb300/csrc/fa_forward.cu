@@ -30,9 +30,10 @@
 //                tile (= TMEM lane r): reads the 64 S columns of a step with
 //                tcgen05.ld, masks, updates (m, l) in base 2 (exp2 via
 //                ex2.approx), writes P as bf16 over the first 32 of them,
-//                rescales its O row when m moved, and runs the epilogue (O_t
-//                leaves TMEM before the next item's Q_t enters). While one tile's
-//                softmax runs, the tensor cores work on the other.
+//                rescales its O row when m moved, moves row r of the next
+//                item's Q_t into TMEM and then runs the epilogue (O_t leaves
+//                TMEM while the next item's first S_t is formed). While one
+//                tile's softmax runs, the tensor cores work on the other.
 // TMEM (512 columns at d = 128): Q0, Q1 (d/2 each, bf16 pairs), S0, S1 (64
 // each), O0, O1 (d each). Scores, probabilities and the accumulators never
 // leave the SM.
@@ -249,7 +250,9 @@ __global__ void __launch_bounds__(384, 1)
             umma_ts_w(tmem + C::COL_O + D * t, tmem + C::COL_S + 64 * t + kk * 8,
                       sdesc_add(b_mn, kk * 2048), kIdescO, (k > 0 || kk > 0) ? 1u : 0u);
         };
-        // Q_0, Q_1 in TMEM (so the previous item's O_t have been read out too)
+        // Q_0, Q_1 in TMEM. (O_t of the previous item may still be being read out:
+        // the O_t += P_t V product that overwrites it waits for P_t, which its
+        // softmax warps write only after that.)
         if (!warp_wait(&bar[C::B_IN], j & 1, wc)) { ok = false; break; }
         if (lane == 0) mbar_arrive(&bar[C::B_KVE + ru % C::STAGES]);  // the Q slot is free
         const int u1 = use_of(0);
@@ -293,7 +296,34 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t ocol = lane_base + C::COL_O + D * t;
     const float sl2 = p.scale_log2;
     int ru = 0, base_t = 0, pvd_t = 0;  // ring uses, steps and finished items of tile t
-    bool ok = true;
+    // Row `row` of Q_t of the item whose Q tiles are ring use `rq` into TMEM: the
+    // row's 16-byte pieces in the 128-byte-swizzled tile (piece j of a chunk row at
+    // j ^ (row % 8)). The previous item's S_t products, the only readers of these
+    // columns, are complete: this warp waited for each of them.
+    auto move_q = [&](int rq) {
+      const int s = rq % C::STAGES;
+      if (!warp_wait(&bar[C::B_KVF + s], (rq / C::STAGES) & 1, wc)) return false;
+      const uint8_t* tile = smem + (t == 0 ? C::OFF_K : C::OFF_V) + s * C::TILE;
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t v[32];
+        const uint8_t* src = tile + c * C::CHUNK + row * 128;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint4 x = *reinterpret_cast<const uint4*>(src + ((q ^ (row & 7)) << 4));
+          v[4 * q] = x.x;
+          v[4 * q + 1] = x.y;
+          v[4 * q + 2] = x.z;
+          v[4 * q + 3] = x.w;
+        }
+        tmem_st32(lane_base + C::COL_Q + (D / 2) * t + 32 * c, v);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bar[C::B_IN]);
+      return true;
+    };
+    bool ok = n_mine == 0 || move_q(0);
     for (int j = 0; ok && j < n_mine; ++j) {
       int qs, bh, nh0, nh1;
       item(j, qs, bh, nh0, nh1);
@@ -302,32 +332,6 @@ __global__ void __launch_bounds__(384, 1)
       const int qg = qs + t * C::BM + row;
       float m_ref = -INFINITY;  // reference maximum of S * scale * log2(e)
       float l_run = 0.f;        // sum of exp2(S * scale * log2(e) - m_ref)
-      // Row `row` of Q_t into TMEM: the row's 16-byte pieces in the 128-byte-swizzled
-      // tile (piece j of a chunk row at j ^ (row % 8)). The previous item's S_t
-      // products, the only readers of these columns, are complete: this warp waited
-      // for each of them.
-      {
-        const int s = ru % C::STAGES;
-        if (!warp_wait(&bar[C::B_KVF + s], (ru / C::STAGES) & 1, wc)) { ok = false; break; }
-        const uint8_t* tile = smem + (t == 0 ? C::OFF_K : C::OFF_V) + s * C::TILE;
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          uint32_t v[32];
-          const uint8_t* src = tile + c * C::CHUNK + row * 128;
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const uint4 x = *reinterpret_cast<const uint4*>(src + ((q ^ (row & 7)) << 4));
-            v[4 * q] = x.x;
-            v[4 * q + 1] = x.y;
-            v[4 * q + 2] = x.z;
-            v[4 * q + 3] = x.w;
-          }
-          tmem_st32(lane_base + C::COL_Q + (D / 2) * t + 32 * c, v);
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(&bar[C::B_IN]);
-      }
       for (int k = 0; ok && k < nh_t; ++k) {
         if (!warp_wait(&bar[C::B_SF + t], (base_t + k) & 1, wc)) {
           ok = false;
@@ -409,6 +413,9 @@ __global__ void __launch_bounds__(384, 1)
         l_run = l_run * corr + (((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7)));
       }
 
+      // The next item's Q_t goes in before this item's O_t comes out, so that the
+      // next item's first S products run while the O rows are written.
+      if (ok && j + 1 < n_mine && !move_q(ru + 1 + nkb)) ok = false;
       // ---------------------------------------------------------- epilogue
       if (ok && nh_t > 0) {
         if (!warp_wait(&bar[C::B_PVD + t], pvd_t & 1, wc)) { ok = false; break; }
