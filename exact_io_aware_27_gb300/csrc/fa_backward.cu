@@ -785,9 +785,16 @@ __device__ __forceinline__ void dq_run(const CUtensorMap& tmQ, const CUtensorMap
       const float nl2 = p.nL2[ws_row];
       const float nd = p.nD[ws_row];
       // Group 0 moves row r of Q into TMEM, group 1 row r of dO. The previous
-      // block's S and dP products, the only readers of these columns, are complete.
+      // block's S and dP products are the only readers of these columns. Group 1
+      // has seen the last of them complete (dP_1 of the last key block). Group 0 has
+      // seen its own, but Q is also read by S_1 of the last key block, issued after
+      // a dQ product that waits for group 1: group 0 waits for that S_1 as well.
       {
         const int s = ru % C::STAGES;
+        if (h == 0 && at >= 1) {
+          if (!warp_wait(&bar[C::B_SF + 1], (gb - 1) & 1, wc)) { ok = false; break; }
+          tc_fence_after();
+        }
         if (!warp_wait(&bar[C::B_KVF + s], (ru / C::STAGES) & 1, wc)) { ok = false; break; }
         tile_row_to_tmem<D>(smem + (h == 0 ? C::OFF_K : C::OFF_V) + s * C::TILE, r,
                             tl + (h == 0 ? C::COL_Q : C::COL_DO));

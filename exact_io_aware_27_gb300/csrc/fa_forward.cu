@@ -71,6 +71,8 @@ struct FwdCfg {
   static constexpr int B_SF = B_IN + 1;          // + tile: S_t of the current step done
   static constexpr int B_PF = B_SF + TILES;      // + tile: P_t written (128 arrivals)
   static constexpr int B_PVD = B_PF + TILES;     // + tile: the tile's last O += P V done
+                                                 // (for a tile with no steps: the item's
+                                                 // products done)
   static constexpr int B_DRAIN = B_PVD + TILES;
   static constexpr int NBAR = B_DRAIN + 1;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;
@@ -280,6 +282,13 @@ __global__ void __launch_bounds__(384, 1)
           if (ok && ((k & 1) || k + 1 == nh))
             umma_commit_w(&bar[C::B_KVE + use_of(k) % C::STAGES]);
         }
+        // A tile with no steps (the second tile of a head's last pair when n mod 256
+        // <= 128) is signalled once the item's products are done, so that its
+        // softmax warps wait for the item's blocks to be consumed before they wait
+        // for the next item's Q slot (whose earlier fill is one of those blocks).
+#pragma unroll
+        for (int t = 0; t < C::TILES; ++t)
+          if (ok && nht[t] == 0) umma_commit_w(&bar[C::B_PVD + t]);
         ru += 1 + nkb;
         base0 += nh0;
         base1 += nh1;
@@ -413,6 +422,13 @@ __global__ void __launch_bounds__(384, 1)
         l_run = l_run * corr + (((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7)));
       }
 
+      // A tile with no steps waits for the end of the item's products first: only
+      // then has the earlier fill of the next item's Q slot surely landed, so that
+      // the slot's barrier is at most one phase behind the wait in move_q.
+      if (ok && nh_t == 0) {
+        if (!warp_wait(&bar[C::B_PVD + t], pvd_t & 1, wc)) { ok = false; break; }
+        ++pvd_t;
+      }
       // The next item's Q_t goes in before this item's O_t comes out, so that the
       // next item's first S products run while the O rows are written.
       if (ok && j + 1 < n_mine && !move_q(ru + 1 + nkb)) ok = false;

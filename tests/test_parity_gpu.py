@@ -94,6 +94,26 @@ def test_edge_shapes(B, H, n, m, d, causal):
     parity.check_heads(Q, K, V, dO, causal, got)
 
 
+# More work items than SMs, so that each persistent CTA runs several items in a row
+# (ring, barrier phases and TMEM reuse carried across items) while the items' second
+# query tile is ragged or empty (n mod 256 <= 128) and key blocks are ragged.
+MANY_ITEMS = [
+    # (B, H, n, m, d, causal)
+    (4, 40, 100, 100, 64, True),
+    (2, 80, 300, 300, 128, True),
+    (3, 60, 130, 170, 128, False),
+    (2, 90, 260, 200, 64, False),
+    (2, 80, 100, 300, 64, True),    # key blocks past every query: no query halves
+]
+
+
+@pytest.mark.parametrize("B,H,n,m,d,causal", MANY_ITEMS)
+def test_several_items_per_cta(B, H, n, m, d, causal):
+    Q, K, V, dO = wl.attention_inputs(B, H, n, m, d, seed=7600 + n + 3 * m + d, qk_std=1.0)
+    got = parity.run_gpu(Q, K, V, dO, causal)
+    parity.check_heads(Q, K, V, dO, causal, got)  # every head: later items of a CTA included
+
+
 # Head dimensions other than 64 and 128 (multiples of 8 up to 128) run the next
 # larger kernel on zero-filled columns. The first two are the shape of the
 # tiled-forward demo of "05_flash_attention.py" (n = 100, d = 32).
