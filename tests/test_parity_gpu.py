@@ -104,6 +104,8 @@ MANY_ITEMS = [
     (3, 60, 130, 170, 128, False),
     (2, 90, 260, 200, 64, False),
     (2, 80, 100, 300, 64, True),    # key blocks past every query: no query halves
+    (3, 60, 90, 333, 128, False),   # empty second tiles, ragged key blocks, d = 128
+    (2, 80, 400, 150, 96, True),    # n > m under causal masking, d = 96
 ]
 
 
