@@ -116,6 +116,17 @@ def test_several_items_per_cta(B, H, n, m, d, causal):
     parity.check_heads(Q, K, V, dO, causal, got)  # every head: later items of a CTA included
 
 
+# Tens of items per CTA: barrier phases wrap many times within one launch.
+@pytest.mark.parametrize("B,H,n,m,d,causal", [
+    (64, 64, 64, 64, 64, True),
+    (32, 64, 130, 100, 128, False),
+])
+def test_many_items_per_cta(B, H, n, m, d, causal):
+    Q, K, V, dO = wl.attention_inputs(B, H, n, m, d, seed=7700 + n + 3 * m + d, qk_std=1.0)
+    got = parity.run_gpu(Q, K, V, dO, causal)
+    parity.check_heads(Q, K, V, dO, causal, got, heads=wl.sample_indices(B * H, 96, 7701 + n))
+
+
 # Head dimensions other than 64 and 128 (multiples of 8 up to 128) run the next
 # larger kernel on zero-filled columns. The first two are the shape of the
 # tiled-forward demo of "05_flash_attention.py" (n = 100, d = 32).
