@@ -116,19 +116,65 @@ def _scale(scale, d):
     return 1.0 / math.sqrt(d) if scale is None else float(scale)
 
 
-def fa_forward(Q, K, V, causal: bool = False, scale: float | None = None, O=None, L=None,
-               stream=None):
-    """O [B,H,n,d] bf16 and L [B,H,n] fp32 (natural-log logsumexp)."""
-    for name, t in (("Q", Q), ("K", K), ("V", V)):
+def _same_device(*ts):
+    dev = ts[0].device
+    for t in ts[1:]:
+        if t.device != dev:
+            raise ValueError("all tensors of a call must be on the same device")
+
+
+def _out(name, t, shape, dtype, device):
+    """A tensor the library writes through its pointer (a caller-provided output):
+    its shape, dtype, device and layout must match exactly, since the library only
+    sees the address."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if (tuple(t.shape) != tuple(shape) or t.dtype != dtype or t.device != device
+            or not t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape "
+                         f"{tuple(shape)} on {device}")
+    return t
+
+
+def _lse(L, B, H, n, device):
+    """The forward's L as an input: fp32 [B,H,n] on the inputs' device."""
+    if (not isinstance(L, torch.Tensor) or L.dtype != torch.float32
+            or tuple(L.shape) != (B, H, n) or not L.is_contiguous() or L.device != device):
+        raise ValueError("L must be a contiguous fp32 [B,H,n] tensor on the inputs' device")
+
+
+def _workspace_bytes(ws, device):
+    if (not isinstance(ws, torch.Tensor) or not ws.is_contiguous() or ws.device != device):
+        raise ValueError("workspace must be a contiguous tensor on the inputs' device")
+    return ws.numel() * ws.element_size()
+
+
+def _attention_inputs(Q, K, V, *more):
+    """Checks Q [B,H,n,d], K and V [B,H,m,d] and any further [B,H,n,d] tensors
+    (O, dO); returns (B, H, n, m, d)."""
+    for name, t in (("Q", Q), ("K", K), ("V", V)) + tuple(more):
         _bf16_4d(name, t)
     B, H, n, d = Q.shape
     m = K.shape[2]
-    if K.shape != (B, H, m, d) or V.shape != (B, H, m, d):
+    if tuple(K.shape) != (B, H, m, d) or tuple(V.shape) != (B, H, m, d):
         raise ValueError("K and V must be [B,H,m,d] with Q's B, H and d")
+    for name, t in more:
+        if tuple(t.shape) != (B, H, n, d):
+            raise ValueError(f"{name} must have Q's shape [B,H,n,d]")
+    _same_device(Q, K, V, *(t for _, t in more))
+    return B, H, n, m, d
+
+
+def fa_forward(Q, K, V, causal: bool = False, scale: float | None = None, O=None, L=None,
+               stream=None):
+    """O [B,H,n,d] bf16 and L [B,H,n] fp32 (natural-log logsumexp)."""
+    B, H, n, m, d = _attention_inputs(Q, K, V)
     if O is None:
         O = torch.empty_like(Q)
     if L is None:
         L = torch.empty((B, H, n), dtype=torch.float32, device=Q.device)
+    _out("O", O, (B, H, n, d), torch.bfloat16, Q.device)
+    _out("L", L, (B, H, n), torch.float32, Q.device)
     rc = lib().fa_forward(Q.data_ptr(), K.data_ptr(), V.data_ptr(), B, H, n, m, d,
                           int(bool(causal)), _scale(scale, d), O.data_ptr(), L.data_ptr(),
                           _stream(Q, stream))
@@ -150,22 +196,25 @@ def alloc_workspace(B, H, n, m, d, device) -> torch.Tensor:
 def fa_backward(Q, K, V, O, L, dO, causal: bool = False, scale: float | None = None, dQ=None,
                 dK=None, dV=None, workspace=None, stream=None):
     """dQ, dK, dV (bf16) for upstream gradient dO, given the forward's O and L."""
-    for name, t in (("Q", Q), ("K", K), ("V", V), ("O", O), ("dO", dO)):
-        _bf16_4d(name, t)
-    B, H, n, d = Q.shape
-    m = K.shape[2]
-    if L.dtype != torch.float32 or tuple(L.shape) != (B, H, n) or not L.is_contiguous():
-        raise ValueError("L must be a contiguous fp32 [B,H,n] CUDA tensor")
-    dQ = torch.empty_like(Q) if dQ is None else dQ
-    dK = torch.empty_like(K) if dK is None else dK
-    dV = torch.empty_like(V) if dV is None else dV
+    B, H, n, m, d = _attention_inputs(Q, K, V, ("O", O), ("dO", dO))
+    _lse(L, B, H, n, Q.device)
+    dQ, dK, dV = _grad_outputs(Q, K, V, dQ, dK, dV)
     if workspace is None:
         workspace = alloc_workspace(B, H, n, m, d, Q.device)
+    ws_bytes = _workspace_bytes(workspace, Q.device)
     rc = lib().fa_backward(Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), L.data_ptr(),
                            dO.data_ptr(), B, H, n, m, d, int(bool(causal)), _scale(scale, d),
                            dQ.data_ptr(), dK.data_ptr(), dV.data_ptr(), workspace.data_ptr(),
-                           workspace.numel() * workspace.element_size(), _stream(Q, stream))
+                           ws_bytes, _stream(Q, stream))
     _check("fa_backward", rc)
+    return dQ, dK, dV
+
+
+def _grad_outputs(Q, K, V, dQ, dK, dV):
+    """dQ, dK, dV: allocated like Q, K, V when not given, else checked against them."""
+    dQ = torch.empty_like(Q) if dQ is None else _out("dQ", dQ, Q.shape, torch.bfloat16, Q.device)
+    dK = torch.empty_like(K) if dK is None else _out("dK", dK, K.shape, torch.bfloat16, K.device)
+    dV = torch.empty_like(V) if dV is None else _out("dV", dV, V.shape, torch.bfloat16, V.device)
     return dQ, dK, dV
 
 
@@ -178,13 +227,9 @@ def fa_backward_noalloc(Q, K, V, O, L, dO, causal: bool = False, scale: float | 
     caller buffer (for callers that cannot allocate device memory; limited to
     problems whose workspace fits in NOALLOC_WORKSPACE_BYTES). Outputs are
     allocated here only when not given."""
-    for name, t in (("Q", Q), ("K", K), ("V", V), ("O", O), ("dO", dO)):
-        _bf16_4d(name, t)
-    B, H, n, d = Q.shape
-    m = K.shape[2]
-    dQ = torch.empty_like(Q) if dQ is None else dQ
-    dK = torch.empty_like(K) if dK is None else dK
-    dV = torch.empty_like(V) if dV is None else dV
+    B, H, n, m, d = _attention_inputs(Q, K, V, ("O", O), ("dO", dO))
+    _lse(L, B, H, n, Q.device)
+    dQ, dK, dV = _grad_outputs(Q, K, V, dQ, dK, dV)
     rc = lib().fa_backward_noalloc(Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(),
                                    L.data_ptr(), dO.data_ptr(), B, H, n, m, d,
                                    int(bool(causal)), _scale(scale, d), dQ.data_ptr(),
@@ -194,34 +239,39 @@ def fa_backward_noalloc(Q, K, V, O, L, dO, causal: bool = False, scale: float | 
 
 
 def fa_backward_preprocess(O, dO, L, workspace, stream=None):
+    for name, t in (("O", O), ("dO", dO)):
+        _bf16_4d(name, t)
+    if tuple(dO.shape) != tuple(O.shape):
+        raise ValueError("dO must have O's shape [B,H,n,d]")
+    _same_device(O, dO)
     B, H, n, d = O.shape
+    _lse(L, B, H, n, O.device)
     rc = lib().fa_backward_preprocess(O.data_ptr(), dO.data_ptr(), L.data_ptr(), B, H, n, d,
-                                      workspace.data_ptr(), workspace.numel(),
+                                      workspace.data_ptr(), _workspace_bytes(workspace, O.device),
                                       _stream(O, stream))
     _check("fa_backward_preprocess", rc)
 
 
 def fa_backward_dkdv(Q, K, V, dO, workspace, causal=False, scale=None, dK=None, dV=None,
                      stream=None):
-    B, H, n, d = Q.shape
-    m = K.shape[2]
-    dK = torch.empty_like(K) if dK is None else dK
-    dV = torch.empty_like(V) if dV is None else dV
+    B, H, n, m, d = _attention_inputs(Q, K, V, ("dO", dO))
+    dK = torch.empty_like(K) if dK is None else _out("dK", dK, K.shape, torch.bfloat16, K.device)
+    dV = torch.empty_like(V) if dV is None else _out("dV", dV, V.shape, torch.bfloat16, V.device)
     rc = lib().fa_backward_dkdv(Q.data_ptr(), K.data_ptr(), V.data_ptr(), dO.data_ptr(), B, H, n,
                                 m, d, int(bool(causal)), _scale(scale, d), dK.data_ptr(),
-                                dV.data_ptr(), workspace.data_ptr(), workspace.numel(),
-                                _stream(Q, stream))
+                                dV.data_ptr(), workspace.data_ptr(),
+                                _workspace_bytes(workspace, Q.device), _stream(Q, stream))
     _check("fa_backward_dkdv", rc)
     return dK, dV
 
 
 def fa_backward_dq(Q, K, V, dO, workspace, causal=False, scale=None, dQ=None, stream=None):
-    B, H, n, d = Q.shape
-    m = K.shape[2]
-    dQ = torch.empty_like(Q) if dQ is None else dQ
+    B, H, n, m, d = _attention_inputs(Q, K, V, ("dO", dO))
+    dQ = torch.empty_like(Q) if dQ is None else _out("dQ", dQ, Q.shape, torch.bfloat16, Q.device)
     rc = lib().fa_backward_dq(Q.data_ptr(), K.data_ptr(), V.data_ptr(), dO.data_ptr(), B, H, n,
                               m, d, int(bool(causal)), _scale(scale, d), dQ.data_ptr(),
-                              workspace.data_ptr(), workspace.numel(), _stream(Q, stream))
+                              workspace.data_ptr(), _workspace_bytes(workspace, Q.device),
+                              _stream(Q, stream))
     _check("fa_backward_dq", rc)
     return dQ
 
@@ -229,15 +279,12 @@ def fa_backward_dq(Q, K, V, dO, workspace, causal=False, scale=None, dQ=None, st
 def fa_backward_grads(Q, K, V, dO, workspace, causal=False, scale=None, dQ=None, dK=None,
                       dV=None, stream=None):
     """dQ, dK, dV in one launch from a workspace fa_backward_preprocess filled."""
-    B, H, n, d = Q.shape
-    m = K.shape[2]
-    dQ = torch.empty_like(Q) if dQ is None else dQ
-    dK = torch.empty_like(K) if dK is None else dK
-    dV = torch.empty_like(V) if dV is None else dV
+    B, H, n, m, d = _attention_inputs(Q, K, V, ("dO", dO))
+    dQ, dK, dV = _grad_outputs(Q, K, V, dQ, dK, dV)
     rc = lib().fa_backward_grads(Q.data_ptr(), K.data_ptr(), V.data_ptr(), dO.data_ptr(), B, H,
                                  n, m, d, int(bool(causal)), _scale(scale, d), dQ.data_ptr(),
                                  dK.data_ptr(), dV.data_ptr(), workspace.data_ptr(),
-                                 workspace.numel(), _stream(Q, stream))
+                                 _workspace_bytes(workspace, Q.device), _stream(Q, stream))
     _check("fa_backward_grads", rc)
     return dQ, dK, dV
 
@@ -250,8 +297,10 @@ def fa_online_softmax_stats(x: torch.Tensor, m=None, l=None, stream=None):
     if not x.is_cuda or not x.is_contiguous():
         raise ValueError("x must be a contiguous CUDA tensor")
     rows, cols = x.shape
-    m = torch.empty(rows, dtype=torch.float32, device=x.device) if m is None else m
-    l = torch.empty(rows, dtype=torch.float32, device=x.device) if l is None else l
+    m = (torch.empty(rows, dtype=torch.float32, device=x.device) if m is None
+         else _out("m", m, (rows,), torch.float32, x.device))
+    l = (torch.empty(rows, dtype=torch.float32, device=x.device) if l is None
+         else _out("l", l, (rows,), torch.float32, x.device))
     rc = lib().fa_online_softmax_stats(x.data_ptr(), rows, cols, m.data_ptr(), l.data_ptr(),
                                        _stream(x, stream))
     _check("fa_online_softmax_stats", rc)
@@ -281,11 +330,14 @@ class Session:
                 raise ValueError(f"{name} must be a contiguous bf16 CPU tensor {(B, H, rows, d)}")
         pin = Q.is_pinned()
         new = (lambda like: torch.empty_like(like, pin_memory=pin))
-        O = new(Q) if O is None else O
-        L = torch.empty((B, H, n), dtype=torch.float32, pin_memory=pin) if L is None else L
-        dQ = new(Q) if dQ is None else dQ
-        dK = new(K) if dK is None else dK
-        dV = new(V) if dV is None else dV
+        cpu = torch.device("cpu")
+        bf = torch.bfloat16
+        O = new(Q) if O is None else _out("O", O, (B, H, n, d), bf, cpu)
+        L = (torch.empty((B, H, n), dtype=torch.float32, pin_memory=pin) if L is None
+             else _out("L", L, (B, H, n), torch.float32, cpu))
+        dQ = new(Q) if dQ is None else _out("dQ", dQ, (B, H, n, d), bf, cpu)
+        dK = new(K) if dK is None else _out("dK", dK, (B, H, m, d), bf, cpu)
+        dV = new(V) if dV is None else _out("dV", dV, (B, H, m, d), bf, cpu)
         rc = lib().fa_session_step(self._handle, Q.data_ptr(), K.data_ptr(), V.data_ptr(),
                                    dO.data_ptr(), int(bool(causal)), _scale(scale, d),
                                    O.data_ptr(), L.data_ptr(), dQ.data_ptr(), dK.data_ptr(),

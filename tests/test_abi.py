@@ -129,6 +129,37 @@ def test_python_binding_rejects_cpu_tensors(lib):
         fa.fa_forward(x, x, x)
 
 
+def test_python_binding_checks_buffers_it_writes_through():
+    """The library sees only addresses, so the binding checks every tensor it hands
+    over for writing (and the forward's L and the workspace) before any call."""
+    import torch
+    from exact_io_aware_27_gb300 import api as A
+    cpu = torch.device("cpu")
+    ok = torch.zeros(2, 3, 5, 8, dtype=torch.bfloat16)
+    assert A._out("O", ok, (2, 3, 5, 8), torch.bfloat16, cpu) is ok
+    bad = [
+        torch.zeros(2, 3, 5, 16, dtype=torch.bfloat16),                  # shape
+        torch.zeros(2, 3, 5, 8, dtype=torch.float32),                     # dtype
+        torch.zeros(2, 3, 8, 5, dtype=torch.bfloat16).transpose(2, 3),    # layout
+        torch.zeros(2, 3, 5, 8, dtype=torch.bfloat16, device="meta"),     # device
+    ]
+    for t in bad:
+        with pytest.raises(ValueError):
+            A._out("O", t, (2, 3, 5, 8), torch.bfloat16, cpu)
+    with pytest.raises(TypeError):
+        A._out("O", None, (2, 3, 5, 8), torch.bfloat16, cpu)
+    A._lse(torch.zeros(2, 3, 5), 2, 3, 5, cpu)
+    for L in (torch.zeros(2, 3, 6), torch.zeros(2, 3, 5, dtype=torch.float64),
+              torch.zeros(2, 3, 5, device="meta")):
+        with pytest.raises(ValueError):
+            A._lse(L, 2, 3, 5, cpu)
+    assert A._workspace_bytes(torch.zeros(10, dtype=torch.float32), cpu) == 40
+    with pytest.raises(ValueError):
+        A._workspace_bytes(torch.zeros(10, device="meta"), cpu)
+    with pytest.raises(ValueError):
+        A._same_device(ok, ok.to("meta"))
+
+
 def test_selftest_argument_errors(lib):
     assert lib.fa_selftest_mma(7, FAKE, FAKE, FAKE, None) == -1
     assert lib.fa_selftest_mma(0, None, FAKE, FAKE, None) == -1
