@@ -1,6 +1,7 @@
 // fa_backward_noalloc: the backward pass for callers that cannot allocate
 // device memory (see include/fa.h). Its workspace is the file-scope array
 // below instead of a caller buffer; everything else is fa_backward's path.
+#include <cstdint>
 #include <mutex>
 
 #include "fa.h"
@@ -47,8 +48,13 @@ extern "C" int fa_backward_noalloc(const void* Q, const void* K, const void* V, 
                        stream);
   }
   if (need > (size_t)FA_NOALLOC_WORKSPACE_BYTES) return FA_ERR_WORKSPACE_TOO_SMALL;
-  // Argument checks that need no device first, so bad calls touch no CUDA state.
+  // Argument checks that need no device first, so bad calls touch no CUDA state
+  // (fa_backward repeats them, with the overlap checks, once the workspace is known).
   if (!Q || !K || !V || !O || !L || !dO || !dQ || !dK || !dV) return FA_ERR_INVALID_ARG;
+  for (const void* p : {Q, K, V, O, dO, static_cast<const void*>(dQ),
+                        static_cast<const void*>(dK), static_cast<const void*>(dV)})
+    if (reinterpret_cast<uintptr_t>(p) & 15u) return FA_ERR_MISALIGNED;
+  if (reinterpret_cast<uintptr_t>(L) & 3u) return FA_ERR_MISALIGNED;
   void* ws = nullptr;
   const int rc = fa::noalloc_workspace(&ws);
   if (rc != FA_OK) return rc;

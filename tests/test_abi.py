@@ -118,6 +118,51 @@ def test_backward_argument_errors(lib):
     assert bwd(scale=0.0) == api.FA_ERR_INVALID_ARG
 
 
+def test_backward_stage_argument_errors(lib):
+    """The stage entry points share fa_backward's checks: missing pointers, head
+    dims, alignment, overlaps and the workspace size, all before any CUDA call."""
+    ws = fa.fa_backward_workspace_size(1, 1, 8, 8, 64)
+    Q, K, V, O, L, dO, dQ, dK, dV, W = [FAKE + (i << 24) for i in range(10)]
+    pre = lambda o=O, do=dO, l=L, d=64, w=W, wb=ws: lib.fa_backward_preprocess(
+        o, do, l, 1, 1, 8, d, w, wb, None)
+    assert pre(o=None) == api.FA_ERR_INVALID_ARG
+    assert pre(l=None) == api.FA_ERR_INVALID_ARG
+    assert pre(d=12) == api.FA_ERR_UNSUPPORTED_HEAD_DIM
+    assert pre(l=L + 2) == api.FA_ERR_MISALIGNED
+    assert pre(wb=ws - 4) == api.FA_ERR_WORKSPACE_TOO_SMALL
+    assert pre(w=O) == api.FA_ERR_INVALID_ARG                  # workspace overlaps O
+    dkdv = lambda k=K, dk=dK, dv=dV, w=W, wb=ws, scale=0.125: lib.fa_backward_dkdv(
+        Q, k, V, dO, 1, 1, 8, 8, 64, 0, scale, dk, dv, w, wb, None)
+    assert dkdv(k=None) == api.FA_ERR_INVALID_ARG
+    assert dkdv(dv=None) == api.FA_ERR_INVALID_ARG
+    assert dkdv(dk=dK + 8) == api.FA_ERR_MISALIGNED
+    assert dkdv(dv=dK) == api.FA_ERR_INVALID_ARG               # dV overlaps dK
+    assert dkdv(dk=K) == api.FA_ERR_INVALID_ARG                # dK overlaps K
+    assert dkdv(wb=0) == api.FA_ERR_WORKSPACE_TOO_SMALL
+    assert dkdv(scale=float("nan")) == api.FA_ERR_INVALID_ARG
+    dq = lambda q=Q, dq_=dQ, w=W, wb=ws: lib.fa_backward_dq(
+        q, K, V, dO, 1, 1, 8, 8, 64, 1, 0.125, dq_, w, wb, None)
+    assert dq(dq_=None) == api.FA_ERR_INVALID_ARG
+    assert dq(dq_=V) == api.FA_ERR_INVALID_ARG                 # dQ overlaps V
+    assert dq(w=dQ) == api.FA_ERR_INVALID_ARG                  # workspace overlaps dQ
+    assert dq(q=Q + 4) == api.FA_ERR_MISALIGNED
+    grads = lambda dq_=dQ, dk=dK, dv=dV, w=W: lib.fa_backward_grads(
+        Q, K, V, dO, 1, 1, 8, 8, 64, 0, 0.125, dq_, dk, dv, w, ws, None)
+    assert grads(dk=None) == api.FA_ERR_INVALID_ARG
+    assert grads(dq_=dV) == api.FA_ERR_INVALID_ARG             # dQ overlaps dV
+    assert grads(w=None) == api.FA_ERR_INVALID_ARG
+
+
+def test_noalloc_argument_errors(lib):
+    Q, K, V, O, L, dO, dQ, dK, dV = [FAKE + (i << 24) for i in range(9)]
+    f = lambda l=L, n=8, dk=dK: lib.fa_backward_noalloc(
+        Q, K, V, O, l, dO, 1, 1, n, 8, 64, 0, 0.125, dQ, dk, dV, None)
+    assert f(l=None) == api.FA_ERR_INVALID_ARG
+    assert f(dk=dK + 2) == api.FA_ERR_MISALIGNED
+    assert f(n=1 << 20) == api.FA_ERR_WORKSPACE_TOO_SMALL     # more than the static buffer
+    assert f(n=0) == api.FA_ERR_INVALID_ARG
+
+
 def test_device_status_needs_pointer(lib):
     assert lib.fa_get_device_status(None) == api.FA_ERR_INVALID_ARG
 
