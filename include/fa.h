@@ -209,6 +209,10 @@ FA_API int fa_online_softmax_stats(const float* x, long long rows, long long col
  * bf16; outputs O, dQ [B,H,n,d], dK, dV [B,H,m,d] bf16 and L [B,H,n] fp32. Scale
  * rules as fa_forward. The session's device must be current. Returns FA_OK or
  * the first error; kernel timeouts are reported by fa_get_device_status().
+ * The host buffers are the caller's and must hold the sizes above: the library
+ * sees only their addresses. A session serves one thread at a time (its streams
+ * and buffer sets are not shared safely by concurrent steps); separate sessions
+ * may run concurrently.
  */
 typedef struct fa_session fa_session;
 FA_API int fa_session_create(int B, int H, int n, int m, int d, int chunk_heads,
