@@ -183,7 +183,7 @@ def run_reference(args):
         return 0
     import oracle
     orc = oracle.default()
-    w = WORKLOAD
+    w = wl.WORKLOADS[getattr(args, "workload", WORKLOAD.name)]  # the arm's own workload
     Q, K, V, dO = wl.workload_inputs(w)
     flat = [t.reshape(w.heads, -1, w.d) for t in (Q, K, V, dO)]
     # Each step: forward + backward of sampled query / key rows of one head,
