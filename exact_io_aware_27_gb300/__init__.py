@@ -10,4 +10,4 @@ from .api import (FAError, FlashAttention, Session, alloc_workspace, fa_backward
                   fa_backward_preprocess,
                   fa_backward_workspace_size, fa_forward, fa_get_device_status,
                   fa_online_softmax_stats,
-                  fa_selftest_mma, flash_attention, lib, status_string, version)
+                  fa_selftest_mma, fa_selftest_wait_timeout, flash_attention, lib, status_string, version)

@@ -54,6 +54,7 @@ SIGNATURES = {
     "fa_get_device_status": (_I, [ctypes.POINTER(_I)]),
     "fa_version": (_I, []),
     "fa_selftest_mma": (_I, [_I, _P, _P, _P, _P]),
+    "fa_selftest_wait_timeout": (_I, [ctypes.c_longlong, _P, _P]),
 }
 
 _lock = threading.Lock()
@@ -372,6 +373,19 @@ def fa_selftest_mma(mode: int, A: torch.Tensor, B: torch.Tensor) -> torch.Tensor
     if rc != 0:
         raise RuntimeError(f"fa_selftest_mma failed ({rc})")
     return D
+
+
+def fa_selftest_wait_timeout(limit_cycles: int, device=None) -> list:
+    """Runs the bounded-wait failure test kernel (see include/fa_selftest.h) on
+    the current stream and returns [ok of warp 0, ok of warp 1] (both 0 when
+    both waits gave up, as they must)."""
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    out = torch.full((2,), -1, dtype=torch.int32, device=dev)
+    rc = lib().fa_selftest_wait_timeout(int(limit_cycles), out.data_ptr(),
+                                        torch.cuda.current_stream(dev).cuda_stream)
+    if rc != 0:
+        raise RuntimeError(f"fa_selftest_wait_timeout failed ({rc})")
+    return [int(x) for x in out.cpu()]
 
 
 class FlashAttention(torch.autograd.Function):

@@ -333,10 +333,11 @@ int fa_online_softmax_stats(const float* x, long long rows, long long cols, floa
 
 int fa_get_device_status(int* status_out) {
   if (!status_out) return FA_ERR_INVALID_ARG;
-  unsigned int f = 0, b = 0;
-  if (forward_read_status(&f) != cudaSuccess || bwd_read_status(&b) != cudaSuccess)
+  unsigned int f = 0, b = 0, t = 0;
+  if (forward_read_status(&f) != cudaSuccess || bwd_read_status(&b) != cudaSuccess ||
+      selftest_read_status(&t) != cudaSuccess)
     return FA_ERR_CUDA;
-  const unsigned int bits = f | b;
+  const unsigned int bits = f | b | t;
   *status_out = (bits & kDeviceTimeoutBit)  ? FA_ERR_DEVICE_TIMEOUT
                 : (bits & kDeviceLayoutBit) ? FA_ERR_UNSUPPORTED_DEVICE
                                             : FA_OK;

@@ -73,6 +73,7 @@ cudaError_t launch_softmax_stats(const float* x, long long rows, long long cols,
 // Read-and-clear of each translation unit's device status word.
 cudaError_t forward_read_status(unsigned int* out);
 cudaError_t bwd_read_status(unsigned int* out);
+cudaError_t selftest_read_status(unsigned int* out);
 
 // Test-only: one tcgen05 GEMM through the same TMA / descriptor paths the
 // attention kernels use (see fa_selftest.h).

@@ -137,7 +137,57 @@ __global__ void __launch_bounds__(128, 1)
   }
 }
 
+// The failure path of the bounded waits, exercised without a fault: nothing ever
+// arrives on either barrier. Warp 0 waits on the first with `limit_cycles`, runs
+// out, raises the CTA abort flag and records kDeviceTimeoutBit; warp 1 waits on
+// the second with the kernels' own limit (about two seconds) and must give up as
+// soon as it sees the abort flag. The CTA holds TMEM during the waits (the
+// attention kernels' situation) and frees it on the way out. No copy and no MMA is
+// ever issued, so nothing is in flight when the waits give up. out[w] = 1 if warp
+// w's wait succeeded, 0 if it gave up.
+__global__ void __launch_bounds__(64, 1)
+    selftest_timeout_kernel(long long limit_cycles, int* __restrict__ out) {
+  __shared__ uint64_t bar[2];
+  __shared__ uint32_t tmem_slot;
+  __shared__ uint32_t abort_word;
+  const WaitCtx wc{&abort_word, &g_selftest_status};
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    abort_word = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&tmem_slot, 32);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const bool ok = warp == 0 ? warp_wait(&bar[0], 0, wc, limit_cycles) : warp_wait(&bar[1], 0, wc);
+  if (lane == 0) out[warp] = ok ? 1 : 0;
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 32);
+  }
+  if (threadIdx.x == 0) {
+    mbar_inval(&bar[0]);
+    mbar_inval(&bar[1]);
+  }
+}
+
 }  // namespace
+
+cudaError_t selftest_read_status(unsigned int* out) {
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_selftest_status, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(g_selftest_status, &zero, sizeof(unsigned int));
+}
 
 cudaError_t launch_selftest_mma(int mode, const void* A, const void* B, float* D,
                                 cudaStream_t s) {
@@ -169,4 +219,17 @@ extern "C" int fa_selftest_mma(int mode, const void* A, const void* B, float* D,
   return fa::launch_selftest_mma(mode, A, B, D, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? 0
              : -6;
+}
+
+extern "C" int fa_selftest_wait_timeout(long long limit_cycles, int* out, void* stream) {
+  if (!out || limit_cycles < 1000 || limit_cycles > fa::kWaitMaxCycles / 4) return -1;
+  if (reinterpret_cast<uintptr_t>(out) & 3) return -3;
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return -6;
+  if (major != 10 || minor != 3) return -4;
+  fa::selftest_timeout_kernel<<<1, 64, 0, static_cast<cudaStream_t>(stream)>>>(limit_cycles, out);
+  return cudaGetLastError() == cudaSuccess ? 0 : -6;
 }

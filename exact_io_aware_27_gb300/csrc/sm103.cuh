@@ -65,8 +65,11 @@ struct WaitCtx {
 };
 
 // Waits until the phase with the given parity of `bar` has completed.
-// Returns false (after raising the abort flag) if it gave up.
-FA_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
+// Returns false (after raising the abort flag) if it gave up: after
+// `max_cycles` of clock64 or kWaitMaxPolls polls, or at once when another
+// thread of the CTA has raised the abort flag.
+FA_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtx& w,
+                      long long max_cycles = kWaitMaxCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
 #pragma unroll 1
@@ -74,7 +77,7 @@ FA_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0u) {
       if (*w.abort_flag) return false;
-      if (clock64() - t0 > kWaitMaxCycles) break;
+      if (clock64() - t0 > max_cycles) break;
     }
   }
   *w.abort_flag = 1u;
@@ -85,8 +88,9 @@ FA_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
 // mbar_wait for a whole warp: every lane polls, and the result is agreed
 // across the warp so that warp-collective instructions (tcgen05.ld/st) that
 // follow are reached by all lanes or by none.
-FA_DEV bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, w));
+FA_DEV bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtx& w,
+                      long long max_cycles = kWaitMaxCycles) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, w, max_cycles));
 }
 
 // Linear block index -> (tile rank within a head, head). Heads are taken in

@@ -31,6 +31,25 @@ extern "C" {
 
 FA_SELFTEST_API int fa_selftest_mma(int mode, const void* A, const void* B, float* D, void* stream);
 
+/*
+ * Exercises the failure path of the library's bounded barrier waits without a
+ * fault (the pages have no counterpart; it backs the device status word that
+ * fa_get_device_status() reports). One CTA of two warps holds 32 TMEM columns
+ * and waits on two shared-memory barriers that nothing ever completes: warp 0
+ * with a limit of `limit_cycles` SM clock cycles, warp 1 with the limit the
+ * attention kernels use (about two seconds). Warp 0 gives up first, raises the
+ * CTA's abort flag and records the timeout bit; warp 1 must then give up at
+ * once. The CTA frees its TMEM and returns; no copy or tensor-core operation is
+ * ever issued, so none is in flight when the waits end.
+ *   out            device int[2], 4-byte aligned: out[w] = 1 if warp w's wait
+ *                  succeeded, 0 if it gave up (both 0 after a correct run)
+ *   limit_cycles   1000 .. 1e9 (about 0.5 ms at 2 GHz is 1e6)
+ * Queued on `stream`; afterwards fa_get_device_status() reports
+ * FA_ERR_DEVICE_TIMEOUT once. Returns 0, -1 (null `out` or limit out of
+ * range), -3 (misaligned), -4 (not compute capability 10.3) or -6 (CUDA error).
+ */
+FA_SELFTEST_API int fa_selftest_wait_timeout(long long limit_cycles, int* out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -26,3 +26,17 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_sessionfinish(session, exitstatus):
+    # The parity figures of every check, for a table of measured errors.
+    path = os.environ.get("FA_PARITY_REPORT")
+    if not path:
+        return
+    try:
+        from tests import parity
+    except Exception:  # the GPU helpers were never imported
+        return
+    import json
+    with open(path, "w") as f:
+        json.dump(parity.REPORTS, f, indent=1)

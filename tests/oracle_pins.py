@@ -4,9 +4,9 @@ Each ``pin_*`` function takes a compiled oracle (``oracle.Oracle``) and raises
 ``AssertionError`` if the oracle disagrees with a value fixed independently of
 it: hand-derived closed forms (``tests/golden``), special cases that reduce to
 a library routine (scipy softmax / logsumexp, torch autograd in fp64), finite
-differences, algebraic invariants, and the tiled algorithm of
-"05_flash_attention.py" (flash_attention_forward / flash_attention_backward)
-restated here in numpy.
+differences, algebraic invariants, and tiling independence: the online-softmax
+merge of per-block statistics and the per-block gradient terms, over shuffled
+even and uneven block partitions, must reproduce the untiled oracle.
 
 The same pins run against mutated copies of the oracle in
 ``test_oracle_mutants.py``; every planted mistake must trip at least one.
@@ -224,82 +224,124 @@ def pin_torch_autograd(orc):
 
 
 # --------------------------------------------------------------------------
-# O8: the tiled algorithm of the pages (numpy restatement) equals the oracle
+# O8: tiling independence. The forward is the online-softmax recurrence
+# ("Flash Attention" notes, section 1.1) in its merge form: for two disjoint
+# sets of keys with statistics (m1, l1), (m2, l2) and unnormalised outputs U1, U2,
+#   M = max(m1, m2),  l = l1 e^(m1 - M) + l2 e^(m2 - M),  U = U1 e^(m1 - M) + U2 e^(m2 - M),
+# so any partition of the score matrix into blocks, merged in any order, must
+# reproduce the oracle. The backward sums the per-block terms of the FA-2
+# gradient formulas ("05_flash_attention.py", flash_attention_backward
+# docstring: P = exp(S - L), dV += P^T dO, dS = P o (dO V^T - D), dQ += s dS K,
+# dK += s dS^T Q), which any visiting order must also reproduce. Blocks are
+# visited in a shuffled order, over even and uneven partitions.
 # --------------------------------------------------------------------------
-def _tiled_forward(Q, K, V, causal, block_q, block_k):
-    """Query-block outer loop, key-block inner loop, running (m, l, O) rescaled
-    by exp(m_old - m_new); key blocks past the diagonal skipped under causal."""
-    n, d = Q.shape
-    mk = K.shape[0]
-    scale = 1.0 / math.sqrt(d)
-    O = np.zeros((n, d))
-    L = np.zeros(n)
-    for qs in range(0, n, block_q):
-        qe = min(qs + block_q, n)
-        Oi = np.zeros((qe - qs, d))
-        mi = np.full(qe - qs, -np.inf)
-        li = np.zeros(qe - qs)
-        for ks in range(0, mk, block_k):
-            if causal and ks > qe - 1:
-                break
-            ke = min(ks + block_k, mk)
-            S = Q[qs:qe] @ K[ks:ke].T * scale
-            if causal:
-                S = np.where(np.arange(ks, ke)[None, :] > np.arange(qs, qe)[:, None], -np.inf, S)
-            m_new = np.maximum(mi, S.max(axis=1))
-            P = np.exp(S - m_new[:, None])
-            corr = np.exp(mi - m_new)
-            li = corr * li + P.sum(axis=1)
-            Oi = corr[:, None] * Oi + P @ V[ks:ke]
-            mi = m_new
-        O[qs:qe] = Oi / li[:, None]
-        L[qs:qe] = mi + np.log(li)
-    return O, L
+def _even_cuts(total, size):
+    """Boundaries of consecutive blocks of `size` rows (the last one ragged)."""
+    return list(range(0, total, size)) + [total]
 
 
-def _tiled_backward(Q, K, V, O, L, dO, causal, block_q, block_k):
-    """Key-block outer loop, query-block inner loop; P rebuilt from L."""
-    n, d = Q.shape
-    scale = 1.0 / math.sqrt(d)
-    D = np.sum(dO * O, axis=1)
-    dQ, dK, dV = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V)
-    for ks in range(0, K.shape[0], block_k):
-        ke = min(ks + block_k, K.shape[0])
-        for qs in range(0, n, block_q):
-            qe = min(qs + block_q, n)
-            if causal and ks > qe - 1:
+def _uneven_cuts(total, rng, lo, hi):
+    """Boundaries of consecutive blocks of random sizes in [lo, hi]."""
+    cuts = [0]
+    while cuts[-1] < total:
+        cuts.append(min(total, cuts[-1] + int(rng.integers(lo, hi + 1))))
+    return cuts
+
+
+def _block_grid(row_cuts, col_cuts, causal):
+    """(query range, key range) pairs holding at least one visible score."""
+    grid = []
+    for r0, r1 in zip(row_cuts, row_cuts[1:]):
+        for c0, c1 in zip(col_cuts, col_cuts[1:]):
+            if causal and c0 > r1 - 1:  # top-left causal: key c visible from query q iff c <= q
                 continue
-            S = Q[qs:qe] @ K[ks:ke].T * scale
-            if causal:
-                S = np.where(np.arange(ks, ke)[None, :] > np.arange(qs, qe)[:, None], -np.inf, S)
-            P = np.exp(S - L[qs:qe, None])
-            dV[ks:ke] += P.T @ dO[qs:qe]
-            dP = dO[qs:qe] @ V[ks:ke].T
-            dS = P * (dP - D[qs:qe, None])
-            dQ[qs:qe] += dS @ K[ks:ke] * scale
-            dK[ks:ke] += dS.T @ Q[qs:qe] * scale
+            grid.append(((r0, r1), (c0, c1)))
+    return grid
+
+
+def _block_scores(Q, K, rows, cols, causal, scale):
+    S = scale * (Q[rows[0]:rows[1]] @ K[cols[0]:cols[1]].T)
+    if causal:
+        hidden = np.arange(*cols)[None, :] > np.arange(*rows)[:, None]
+        S = np.where(hidden, -np.inf, S)
+    return S
+
+
+def _merge_weights(m_a, m_b):
+    """e^(m_a - M), e^(m_b - M) for M = max(m_a, m_b); 0 for a side still at -inf."""
+    M = np.maximum(m_a, m_b)
+    finite = np.isfinite(M)
+    safe = np.where(finite, M, 0.0)
+    w_a = np.where(np.isfinite(m_a), np.exp(np.where(np.isfinite(m_a), m_a, 0.0) - safe), 0.0)
+    w_b = np.where(np.isfinite(m_b), np.exp(np.where(np.isfinite(m_b), m_b, 0.0) - safe), 0.0)
+    return M, w_a, w_b
+
+
+def _tiled_forward(Q, K, V, causal, row_cuts, col_cuts, rng):
+    n, d = Q.shape
+    scale = 1.0 / math.sqrt(d)
+    run_m = np.full(n, -np.inf)      # running maximum per query
+    run_l = np.zeros(n)              # exp-sum relative to run_m
+    run_u = np.zeros((n, d))         # unnormalised output relative to run_m
+    grid = _block_grid(row_cuts, col_cuts, causal)
+    for g in rng.permutation(len(grid)):
+        rows, cols = grid[g]
+        S = _block_scores(Q, K, rows, cols, causal, scale)
+        blk_m = S.max(axis=1)        # -inf for a row with no visible key in the block
+        E = np.exp(S - np.where(np.isfinite(blk_m), blk_m, 0.0)[:, None])
+        blk_l, blk_u = E.sum(axis=1), E @ V[cols[0]:cols[1]]
+        sl = slice(*rows)
+        M, w_run, w_blk = _merge_weights(run_m[sl], blk_m)
+        run_l[sl] = run_l[sl] * w_run + blk_l * w_blk
+        run_u[sl] = run_u[sl] * w_run[:, None] + blk_u * w_blk[:, None]
+        run_m[sl] = M
+    return run_u / run_l[:, None], run_m + np.log(run_l)
+
+
+def _tiled_backward(Q, K, V, O, L, dO, causal, row_cuts, col_cuts, rng):
+    d = Q.shape[1]
+    scale = 1.0 / math.sqrt(d)
+    Drow = np.einsum("ij,ij->i", dO, O)
+    dQ, dK, dV = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V)
+    grid = _block_grid(row_cuts, col_cuts, causal)
+    for g in rng.permutation(len(grid)):
+        rows, cols = grid[g]
+        qs, ks = slice(*rows), slice(*cols)
+        P = np.exp(_block_scores(Q, K, rows, cols, causal, scale) - L[qs, None])
+        dS = P * (dO[qs] @ V[ks].T - Drow[qs, None])
+        dQ[qs] += scale * (dS @ K[ks])
+        dK[ks] += scale * (dS.T @ Q[qs])
+        dV[ks] += P.T @ dO[qs]
     return dQ, dK, dV
 
 
 def pin_tiled_page1(orc):
     rng = _rng(9)
+    # the pages' forward demo shape: n = 100, d = 32, 16-query x 24-key blocks
     n, d = 100, 32
     Q, K, V = (rng.standard_normal((n, d)) for _ in range(3))
+    parts = [("16x24", _even_cuts(n, 16), _even_cuts(n, 24)),
+             ("uneven", _uneven_cuts(n, rng, 3, 29), _uneven_cuts(n, rng, 2, 31))]
     for causal in (False, True):
-        O_t, L_t = _tiled_forward(Q, K, V, causal, 16, 24)
         O, L = orc.forward(Q, K, V, causal)
-        _close(O, O_t, 1e-12, 1e-12, f"tiled forward O causal={causal}")
-        _close(L, L_t, 1e-12, 1e-12, f"tiled forward L causal={causal}")
+        for tag, rc, cc in parts:
+            O_t, L_t = _tiled_forward(Q, K, V, causal, rc, cc, rng)
+            _close(O, O_t, 1e-12, 1e-12, f"tiled forward O {tag} causal={causal}")
+            _close(L, L_t, 1e-12, 1e-12, f"tiled forward L {tag} causal={causal}")
+    # the pages' backward demo: n = 70, d = 16, loss sum(O**2) so dO = 2 O
     n, d = 70, 16
     Q, K, V = (rng.standard_normal((n, d)) for _ in range(3))
+    parts = [("16x16", _even_cuts(n, 16), _even_cuts(n, 16)),
+             ("uneven", _uneven_cuts(n, rng, 2, 23), _uneven_cuts(n, rng, 4, 19))]
     for causal in (False, True):
         O, L = orc.forward(Q, K, V, causal)
-        dO = 2.0 * O  # loss sum(O**2)
-        dQ_t, dK_t, dV_t = _tiled_backward(Q, K, V, O, L, dO, causal, 16, 16)
+        dO = 2.0 * O
         dQ, dK, dV, _ = orc.backward(Q, K, V, dO, causal)
-        _close(dQ, dQ_t, 1e-11, 1e-12, f"tiled backward dQ causal={causal}")
-        _close(dK, dK_t, 1e-11, 1e-12, f"tiled backward dK causal={causal}")
-        _close(dV, dV_t, 1e-11, 1e-12, f"tiled backward dV causal={causal}")
+        for tag, rc, cc in parts:
+            dQ_t, dK_t, dV_t = _tiled_backward(Q, K, V, O, L, dO, causal, rc, cc, rng)
+            _close(dQ, dQ_t, 1e-11, 1e-12, f"tiled backward dQ {tag} causal={causal}")
+            _close(dK, dK_t, 1e-11, 1e-12, f"tiled backward dK {tag} causal={causal}")
+            _close(dV, dV_t, 1e-11, 1e-12, f"tiled backward dV {tag} causal={causal}")
 
 
 # --------------------------------------------------------------------------

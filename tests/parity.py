@@ -1,14 +1,23 @@
 """Helpers for comparing the CUDA path with the fp64 oracle.
 
 Tolerances (fp32 accumulation, bf16 inputs and outputs):
-  O   max-abs error  <= 1e-2 beyond O's own rounding to bf16: the kernel must
-      return bf16, and rounding even the exact value costs up to half a bf16
-      ulp (2^-8 |O|, e.g. 0.0156 for |O| in [4, 8)), so each element may differ
-      from the fp64 value by 1e-2 + half_ulp_bf16(O_ref)
+  O   max-abs error  <= 1e-2, raw, on every element whose exact value has
+      |O_ref| < 2 (there half a bf16 ulp is at most 2^-8 = 0.0039, so the raw
+      bound is attainable). An element with |O_ref| >= 2 cannot always meet a
+      raw 1e-2 in bf16: rounding even the exact value costs up to half a bf16
+      ulp (2^-8 |O|, e.g. 0.0156 for |O| in [4, 8)). Such elements (the peaked
+      cross-attention workload has |O| near 5, and the first causal rows can
+      reach 2) may differ by 1e-2 + half_ulp_bf16(O_ref).
   L   max-abs error  <= 2e-3   (natural log)
   dQ, dK, dV  relative Frobenius error ||g - r||_F / ||r||_F <= 1e-2
+
+Every check records its figures (the raw O error over all elements too) in
+REPORTS, which tests/conftest.py writes out as JSON when FA_PARITY_REPORT names
+a file.
 """
 from __future__ import annotations
+
+import os
 
 import numpy as np
 import torch
@@ -32,9 +41,45 @@ def half_ulp_bf16(x) -> np.ndarray:
     return np.exp2(e - 8)
 
 
+O_RAW_BELOW = 2.0  # |O_ref| below this: the raw bound applies
+
+REPORTS = []  # one dict per check: label and figures
+
+
+def o_errors(g, r) -> dict:
+    """O error figures: raw max-abs over all elements and over |r| < 2, and the
+    error beyond r's own bf16 rounding over |r| >= 2 (with their count)."""
+    g = np.asarray(g, dtype=np.float64)
+    r = np.asarray(r, dtype=np.float64)
+    diff = np.abs(g - r)
+    small = np.abs(r) < O_RAW_BELOW
+    big = ~small
+    return {
+        "O_raw": float(diff.max()) if diff.size else 0.0,
+        "O_raw_lt2": float(diff[small].max()) if small.any() else 0.0,
+        "O_ge2_beyond_rounding": float((diff - half_ulp_bf16(r))[big].max()) if big.any() else 0.0,
+        "O_n_ge2": int(big.sum()),
+    }
+
+
 def o_error(g, r) -> float:
-    """Max over elements of |g - r| in excess of r's own bf16 rounding."""
-    return float(np.max(np.abs(np.asarray(g) - r) - half_ulp_bf16(r)))
+    """The checked O figure: raw max-abs on |r| < 2, beyond bf16 rounding on |r| >= 2."""
+    e = o_errors(g, r)
+    return max(e["O_raw_lt2"], e["O_ge2_beyond_rounding"])
+
+
+def _merge(report, errs):
+    for key, val in errs.items():
+        if key == "O_n_ge2":
+            report[key] = report.get(key, 0) + val
+        else:
+            report[key] = max(report.get(key, 0.0), val)
+
+
+def _record(report, label):
+    if label is None:
+        label = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+    REPORTS.append({"label": label, **report})
 
 
 def rel_fro(g, r) -> float:
@@ -52,7 +97,7 @@ def run_gpu(Q, K, V, dO, causal, scale=None, device="cuda"):
     return {"O": f64(O), "L": f64(L), "dQ": f64(dQ), "dK": f64(dK), "dV": f64(dV)}
 
 
-def check_heads(Q, K, V, dO, causal, got, heads=None, scale=None):
+def check_heads(Q, K, V, dO, causal, got, heads=None, scale=None, label=None):
     """Full-row comparison on every head (or the listed flat head indices)."""
     B, H, n, d = Q.shape
     m = K.shape[2]
@@ -65,20 +110,19 @@ def check_heads(Q, K, V, dO, causal, got, heads=None, scale=None):
         O_r, L_r = oracle.forward(q, k, v, causal, scale)
         dQ_r, dK_r, dV_r, _ = oracle.backward(q, k, v, do, causal, scale)
         errs = {
-            "O": o_error(g["O"][h], O_r),
-            "O_raw": float(np.max(np.abs(g["O"][h] - O_r))),
+            **o_errors(g["O"][h], O_r),
             "L": float(np.max(np.abs(g["L"][h] - L_r))),
             "dQ": rel_fro(g["dQ"][h], dQ_r),
             "dK": rel_fro(g["dK"][h], dK_r),
             "dV": rel_fro(g["dV"][h], dV_r),
         }
-        for key, val in errs.items():
-            report[key] = max(report.get(key, 0.0), val)
+        _merge(report, errs)
+    _record(report, label)
     assert_within(report)
     return report
 
 
-def check_sampled(Q, K, V, dO, causal, got, heads, q_rows, k_rows, scale=None):
+def check_sampled(Q, K, V, dO, causal, got, heads, q_rows, k_rows, scale=None, label=None):
     """Sampled rows of sampled heads (for workloads the full oracle is too slow on)."""
     B, H, n, d = Q.shape
     flat = [t.reshape(B * H, -1, d) for t in (Q, K, V, dO)]
@@ -90,23 +134,25 @@ def check_sampled(Q, K, V, dO, causal, got, heads, q_rows, k_rows, scale=None):
         O_r, L_r = orc.forward_rows(q, k, v, q_rows, causal, scale)
         dQ_r, dK_r, dV_r, _ = orc.backward_rows(q, k, v, do, q_rows, k_rows, causal, scale)
         errs = {
-            "O": o_error(g["O"][h][q_rows], O_r),
-            "O_raw": float(np.max(np.abs(g["O"][h][q_rows] - O_r))),
+            **o_errors(g["O"][h][q_rows], O_r),
             "L": float(np.max(np.abs(g["L"][h][q_rows] - L_r))),
             "dQ": rel_fro(g["dQ"][h][q_rows], dQ_r),
             "dK": rel_fro(g["dK"][h][k_rows], dK_r),
             "dV": rel_fro(g["dV"][h][k_rows], dV_r),
         }
-        for key, val in errs.items():
-            report[key] = max(report.get(key, 0.0), val)
+        _merge(report, errs)
+    _record(report, label)
     assert_within(report)
     return report
 
 
 def assert_within(report):
     bad = []
-    if not report["O"] <= O_MAXABS:
-        bad.append(f"O max-abs beyond bf16 output rounding {report['O']:.3e} > {O_MAXABS}")
+    if not report["O_raw_lt2"] <= O_MAXABS:
+        bad.append(f"O max-abs (|O| < {O_RAW_BELOW}) {report['O_raw_lt2']:.3e} > {O_MAXABS}")
+    if not report["O_ge2_beyond_rounding"] <= O_MAXABS:
+        bad.append(f"O max-abs beyond bf16 rounding (|O| >= {O_RAW_BELOW}) "
+                   f"{report['O_ge2_beyond_rounding']:.3e} > {O_MAXABS}")
     if not report["L"] <= L_MAXABS:
         bad.append(f"L max-abs {report['L']:.3e} > {L_MAXABS}")
     for k in ("dQ", "dK", "dV"):

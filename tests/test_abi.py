@@ -209,6 +209,10 @@ def test_selftest_argument_errors(lib):
     assert lib.fa_selftest_mma(7, FAKE, FAKE, FAKE, None) == -1
     assert lib.fa_selftest_mma(0, None, FAKE, FAKE, None) == -1
     assert lib.fa_selftest_mma(0, FAKE + 2, FAKE, FAKE, None) == -3
+    assert lib.fa_selftest_wait_timeout(10**6, None, None) == -1
+    assert lib.fa_selftest_wait_timeout(999, FAKE, None) == -1
+    assert lib.fa_selftest_wait_timeout(2 * 10**9, FAKE, None) == -1
+    assert lib.fa_selftest_wait_timeout(10**6, FAKE + 2, None) == -3
 
 
 def test_online_softmax_argument_errors(lib):
