@@ -559,6 +559,100 @@ def run_online_softmax(args):
     return 0
 
 
+IO_SIZES = (1024, 4096, 16384)
+IO_QUERY_ROWS = 65536  # the batched rows: B*H*n query rows in total
+
+
+def io_configs():
+    """(label, B, H, n, d) of the IO comparison: one head at each n (the pages'
+    per-head model) and a batch of heads holding IO_QUERY_ROWS query rows."""
+    out = []
+    for n in IO_SIZES:
+        out.append((f"one_head_n{n}_d128", 1, 1, n, 128))
+        out.append((f"h{IO_QUERY_ROWS // n}_n{n}_d128", 1, IO_QUERY_ROWS // n, n, 128))
+    return out
+
+
+def io_model_bytes(B, H, n, m, d):
+    """Algorithmic memory traffic of one forward, non-causal, in bytes:
+    standard = read Q, K, V; write S; read S; write P; read P; write O, L (the
+    pages' 4 n m element accesses of S and P on top of the inputs and outputs);
+    tiled = read Q, K, V; write O, L."""
+    heads = B * H
+    io = heads * ((2 * n + 2 * m) * d * 2 + n * 4)
+    return {"standard": io + heads * 4 * n * m * 2, "tiled": io}
+
+
+def run_io_compare(args):
+    """The pages' IO comparison on the GPU: the materialised standard path
+    (fa_standard_forward: S and P written to memory) against the tiled forward
+    (fa_forward) on the same inputs, non-causal, d = 128. Times are CUDA-event
+    medians with L2 flushed before every launch; memory is the peak the path
+    allocates beyond its inputs. DRAM bytes per kernel come from ncu."""
+    import exact_io_aware_27_gb300 as fa
+
+    world, rank, local = _dist()
+    if rank != 0:
+        return 0
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    rows = []
+    for label, B, H, n, d in io_configs():
+        Q, K, V, _ = wl.attention_inputs(B, H, n, n, d, seed=9000 + n + H, qk_std=1.0)
+        q, k, v = (t.to(dev) for t in (Q, K, V))
+        res = {"config": label, "B": B, "H": H, "n": n, "m": n, "d": d,
+               "model_bytes": io_model_bytes(B, H, n, n, d)}
+        for path in ("standard", "tiled"):
+            torch.cuda.synchronize(dev)
+            base = torch.cuda.memory_allocated(dev)
+            torch.cuda.reset_peak_memory_stats(dev)
+
+            def call():
+                if path == "standard":
+                    return fa.fa_standard_forward(q, k, v, False)
+                return fa.fa_forward(q, k, v, False)
+
+            out = call()
+            torch.cuda.synchronize(dev)
+            peak = torch.cuda.max_memory_allocated(dev) - base
+            out_bytes = B * H * n * (d * 2 + 4)  # O and L, which both paths return
+            del out
+            times = []
+            for _ in range(max(3, args.warmup) + min(args.steps, 50)):
+                flush.fill_(1)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                o = call()
+                e1.record(stream)
+                torch.cuda.synchronize(dev)
+                times.append(e0.elapsed_time(e1))
+                del o
+            t = statistics.median(times[max(3, args.warmup):])
+            res[path] = {"ms": t, "peak_alloc_bytes": peak, "extra_bytes": peak - out_bytes}
+        res["time_ratio"] = res["standard"]["ms"] / res["tiled"]["ms"]
+        rows.append(res)
+        del q, k, v
+        torch.cuda.empty_cache()
+    if fa.fa_get_device_status() != 0:
+        raise RuntimeError("device barrier timeout during the IO comparison")
+    big = rows[-1]
+    line = {
+        "metric": "IO comparison: time of the materialised standard forward / the tiled forward",
+        "value": big["time_ratio"], "unit": "x", "n_gpus": 1, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": big["tiled"]["ms"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": big["config"], "l2": "L2 flushed (512 MiB written) before every launch",
+                   "causal": False},
+        "rows": rows, "e2e": None, "gpu_launches": 4 * len(rows) * (max(3, args.warmup) + args.steps + 1),
+        "cpu_baseline": None,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -576,12 +670,16 @@ def main():
                     help="skip the end-to-end host-buffer loop (profiling runs)")
     ap.add_argument("--cpu-heads", type=int, default=4,
                     help="heads of the workload the oracle baseline times")
-    ap.add_argument("--kernel", choices=["attention", "online_softmax"], default="attention",
-                    help="the attention step (default) or the standalone online-softmax "
-                         "statistics kernel")
+    ap.add_argument("--kernel", choices=["attention", "online_softmax", "io_compare"],
+                    default="attention",
+                    help="the attention step (default), the standalone online-softmax "
+                         "statistics kernel, or the IO comparison of the materialised "
+                         "standard forward against the tiled one")
     args = ap.parse_args()
     if args.kernel == "online_softmax":
         return run_online_softmax(args)
+    if args.kernel == "io_compare":
+        return run_io_compare(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -9,5 +9,5 @@ from .api import (FAError, FlashAttention, Session, alloc_workspace, fa_backward
                   fa_backward_dkdv, fa_backward_dq, fa_backward_grads, fa_backward_noalloc,
                   fa_backward_preprocess,
                   fa_backward_workspace_size, fa_forward, fa_get_device_status,
-                  fa_online_softmax_stats,
+                  fa_online_softmax_stats, fa_standard_forward, fa_standard_matrix_bytes,
                   fa_selftest_mma, fa_selftest_wait_timeout, flash_attention, lib, status_string, version)

@@ -20,7 +20,7 @@ BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIBRARY = os.path.join(PKG_DIR, "libfa_gb300.so")
 
 SOURCES = ["fa_api.cu", "fa_forward.cu", "fa_backward.cu", "fa_softmax.cu", "fa_selftest.cu",
-           "fa_noalloc.cu", "fa_session.cu"]
+           "fa_noalloc.cu", "fa_session.cu", "fa_standard.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
                      "-Xcompiler", "-fvisibility=hidden", "-I" + INCLUDE, "-I" + CSRC]

@@ -47,6 +47,8 @@ SIGNATURES = {
     "fa_backward_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P,
                                  _P, _P]),
     "fa_online_softmax_stats": (_I, [_P, ctypes.c_longlong, ctypes.c_longlong, _P, _P, _P]),
+    "fa_standard_matrix_bytes": (_S, [_I, _I, _I, _I]),
+    "fa_standard_forward": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P]),
     "fa_session_create": (_I, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_P)]),
     "fa_session_destroy": (None, [_P]),
     "fa_session_step": (_I, [_P, _P, _P, _P, _P, _I, _F, _P, _P, _P, _P, _P]),
@@ -181,6 +183,37 @@ def fa_forward(Q, K, V, causal: bool = False, scale: float | None = None, O=None
                           _stream(Q, stream))
     _check("fa_forward", rc)
     return O, L
+
+
+def fa_standard_matrix_bytes(B: int, H: int, n: int, m: int) -> int:
+    """Bytes of one of the S, P matrices of fa_standard_forward (bf16 [B,H,n,m_pad])."""
+    return int(lib().fa_standard_matrix_bytes(B, H, n, m))
+
+
+def fa_standard_forward(Q, K, V, causal: bool = False, scale: float | None = None, S=None,
+                        P=None, O=None, L=None, stream=None):
+    """Materialised standard attention: (O, L, S, P) with S = scale Q K^T and
+    P = softmax(S) as bf16 [B,H,n,m_pad] matrices in device memory (m_pad = m
+    rounded up to 64; the columns past m are 0)."""
+    B, H, n, m, d = _attention_inputs(Q, K, V)
+    m_pad = (m + 63) // 64 * 64
+    if S is None:
+        S = torch.empty((B, H, n, m_pad), dtype=torch.bfloat16, device=Q.device)
+    if P is None:
+        P = torch.empty((B, H, n, m_pad), dtype=torch.bfloat16, device=Q.device)
+    if O is None:
+        O = torch.empty_like(Q)
+    if L is None:
+        L = torch.empty((B, H, n), dtype=torch.float32, device=Q.device)
+    _out("S", S, (B, H, n, m_pad), torch.bfloat16, Q.device)
+    _out("P", P, (B, H, n, m_pad), torch.bfloat16, Q.device)
+    _out("O", O, (B, H, n, d), torch.bfloat16, Q.device)
+    _out("L", L, (B, H, n), torch.float32, Q.device)
+    rc = lib().fa_standard_forward(Q.data_ptr(), K.data_ptr(), V.data_ptr(), B, H, n, m, d,
+                                   int(bool(causal)), _scale(scale, d), S.data_ptr(), P.data_ptr(),
+                                   O.data_ptr(), L.data_ptr(), _stream(Q, stream))
+    _check("fa_standard_forward", rc)
+    return O, L, S, P
 
 
 def fa_backward_workspace_size(B: int, H: int, n: int, m: int, d: int) -> int:

@@ -331,13 +331,60 @@ int fa_online_softmax_stats(const float* x, long long rows, long long cols, floa
   return from_cuda(launch_softmax_stats(x, rows, cols, m, l, static_cast<cudaStream_t>(stream)));
 }
 
+size_t fa_standard_matrix_bytes(int B, int H, int n, int m) {
+  if (B < 1 || H < 1 || n < 1 || m < 1 || n > kMaxSeq || m > kMaxSeq) return 0;
+  return (size_t)B * H * n * round_up(m, kStdColAlign) * 2;
+}
+
+int fa_standard_forward(const void* Q, const void* K, const void* V, int B, int H, int n, int m,
+                        int d, int causal, float scale, void* S, void* P, void* O, float* L,
+                        void* stream) {
+  int rc = check_sizes(B, H, n, m, d);
+  if (rc != FA_OK) return rc;
+  if ((rc = check_scale(scale)) != FA_OK) return rc;
+  if (!Q || !K || !V || !S || !P || !O || !L) return FA_ERR_INVALID_ARG;
+  if (ceil_div(n, 128) > 65535) return FA_ERR_INVALID_ARG;  // query tiles: one grid row each
+  const void* bf16s[] = {Q, K, V, S, P, O};
+  for (const void* ptr : bf16s)
+    if (!aligned(ptr, 16)) return FA_ERR_MISALIGNED;
+  if (!aligned(L, 4)) return FA_ERR_MISALIGNED;
+  const size_t qn = (size_t)B * H * n * d * 2, km = (size_t)B * H * m * d * 2;
+  const size_t sp = fa_standard_matrix_bytes(B, H, n, m);
+  const Range ins[] = {range_of(Q, qn), range_of(K, km), range_of(V, km)};
+  const Range outs[] = {range_of(S, sp), range_of(P, sp), range_of(O, qn),
+                        range_of(L, (size_t)B * H * n * 4)};
+  for (const Range& o : outs)
+    for (const Range& i : ins)
+      if (overlap(o, i)) return FA_ERR_INVALID_ARG;
+  for (int x = 0; x < 4; ++x)
+    for (int y = x + 1; y < 4; ++y)
+      if (overlap(outs[x], outs[y])) return FA_ERR_INVALID_ARG;
+  if ((rc = check_device()) != FA_OK) return rc;
+  StdArgs a;
+  a.Q = Q;
+  a.K = K;
+  a.V = V;
+  a.S = S;
+  a.P = P;
+  a.O = O;
+  a.L = L;
+  a.BH = B * H;
+  a.n = n;
+  a.m = m;
+  a.m_pad = round_up(m, kStdColAlign);
+  a.d = d;
+  a.causal = causal ? 1 : 0;
+  a.scale = scale;
+  return from_cuda(launch_standard(a, static_cast<cudaStream_t>(stream)));
+}
+
 int fa_get_device_status(int* status_out) {
   if (!status_out) return FA_ERR_INVALID_ARG;
-  unsigned int f = 0, b = 0, t = 0;
+  unsigned int f = 0, b = 0, t = 0, sd = 0;
   if (forward_read_status(&f) != cudaSuccess || bwd_read_status(&b) != cudaSuccess ||
-      selftest_read_status(&t) != cudaSuccess)
+      selftest_read_status(&t) != cudaSuccess || standard_read_status(&sd) != cudaSuccess)
     return FA_ERR_CUDA;
-  const unsigned int bits = f | b | t;
+  const unsigned int bits = f | b | t | sd;
   *status_out = (bits & kDeviceTimeoutBit)  ? FA_ERR_DEVICE_TIMEOUT
                 : (bits & kDeviceLayoutBit) ? FA_ERR_UNSUPPORTED_DEVICE
                                             : FA_OK;

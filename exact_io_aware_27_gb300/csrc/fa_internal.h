@@ -58,7 +58,19 @@ struct BwdArgs {
   float scale;
 };
 
+// Materialised standard attention (the baseline of the IO comparison): S and P
+// are bf16 [BH, n, m_pad] matrices in memory, m_pad = m rounded up to 64.
+constexpr int kStdColAlign = 64;
+struct StdArgs {
+  const void *Q, *K, *V;
+  void *S, *P, *O;
+  float* L;
+  int BH, n, m, m_pad, d, causal;
+  float scale;
+};
+
 // Kernel launches (return the launch's cudaError_t).
+cudaError_t launch_standard(const StdArgs& a, cudaStream_t s);
 cudaError_t launch_forward(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, cudaStream_t s);
@@ -74,6 +86,7 @@ cudaError_t launch_softmax_stats(const float* x, long long rows, long long cols,
 cudaError_t forward_read_status(unsigned int* out);
 cudaError_t bwd_read_status(unsigned int* out);
 cudaError_t selftest_read_status(unsigned int* out);
+cudaError_t standard_read_status(unsigned int* out);
 
 // Test-only: one tcgen05 GEMM through the same TMA / descriptor paths the
 // attention kernels use (see fa_selftest.h).

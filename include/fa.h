@@ -165,6 +165,34 @@ FA_API int fa_backward_noalloc(const void* Q, const void* K, const void* V, cons
                                void* stream);
 
 /*
+ * Standard (materialised) attention, the baseline of the pages' IO comparison
+ * ("05_flash_attention.py", standard_attention and demo_memory): the same O and
+ * L as fa_forward, computed the way the pages' standard implementation does it,
+ * with the n x m score and probability matrices written to memory.
+ *   S = scale * Q K^T  for every (query, key) pair, fp32 accumulation, rounded
+ *                      to bf16 and stored to S
+ *   P = softmax(S)     per row of the stored S, with the causal mask (key k
+ *                      visible from query q iff k <= q, top-left) applied here;
+ *                      computed in fp32, rounded to bf16 and stored to P;
+ *                      L = logsumexp of the row (natural log, fp32)
+ *   O = P V            fp32 accumulation, rounded to bf16
+ * Causal masking skips no work: S is computed and stored in full. Q, K, V, O and
+ * L are laid out as for fa_forward. S and P are caller-owned device buffers of
+ * fa_standard_matrix_bytes(B, H, n, m) bytes each, bf16 [B, H, n, m_pad] with
+ * m_pad = m rounded up to a multiple of 64; columns past m hold 0 in P (and in
+ * S), and their contents on entry do not matter. Because S and P are rounded to
+ * bf16, O and L carry the extra error of those roundings (up to 2^-8 of each
+ * score and weight). Same size, alignment (16 bytes; L 4 bytes), aliasing
+ * (no output may overlap an input or another output) and device rules as
+ * fa_forward; three kernel launches on `stream`. Returns FA_OK or a negative
+ * fa_status.
+ */
+FA_API size_t fa_standard_matrix_bytes(int B, int H, int n, int m);
+FA_API int fa_standard_forward(const void* Q, const void* K, const void* V, int B, int H, int n,
+                               int m, int d, int causal, float scale, void* S, void* P, void* O,
+                               float* L, void* stream);
+
+/*
  * Online softmax statistics ("05_flash_attention.py", online_softmax_stats;
  * "Flash Attention" notes, section 1.1), the building block of the forward pass
  * on its own: for each row of the row-major fp32 matrix x [rows, cols] (device

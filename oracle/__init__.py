@@ -89,6 +89,10 @@ class Oracle:
             ctypes.c_int, ctypes.c_double, _lp, ctypes.c_long, _lp, ctypes.c_long, _dptr,
             _dptr, _dptr, _dptr]
         lib.oracle_attention_backward_rows.restype = ctypes.c_int
+        lib.oracle_attention_probabilities.argtypes = [
+            _dptr, _dptr, ctypes.c_long, ctypes.c_long, ctypes.c_long, ctypes.c_int,
+            ctypes.c_double, _dptr, _dptr]
+        lib.oracle_attention_probabilities.restype = ctypes.c_int
         self._lib = lib
         self.path = path
 
@@ -136,6 +140,24 @@ class Oracle:
             if rc != 0:
                 raise ValueError("oracle_attention_forward: bad arguments")
         return O.reshape(*lead, n, d), L.reshape(*lead, n)
+
+    def probabilities(self, Q, K, causal: bool = False, scale: float | None = None):
+        """S [..., n, m] (-inf where masked) and P = softmax(S) [..., n, m] per head."""
+        q, lead = self._heads(Q)
+        k, _ = self._heads(K)
+        nh, n, d = q.shape
+        m = k.shape[1]
+        if scale is None:
+            scale = 1.0 / np.sqrt(d)
+        S = np.empty((nh, n, m))
+        P = np.empty((nh, n, m))
+        for h in range(nh):
+            rc = self._lib.oracle_attention_probabilities(
+                _as_ptr(q[h]), _as_ptr(k[h]), n, m, d, int(bool(causal)), float(scale),
+                _as_ptr(S[h]), _as_ptr(P[h]))
+            if rc != 0:
+                raise ValueError("oracle_attention_probabilities: bad arguments")
+        return S.reshape(*lead, n, m), P.reshape(*lead, n, m)
 
     def backward(self, Q, K, V, dO, causal: bool = False, scale: float | None = None):
         """dQ, dK, dV and D (= sum_j P_ij dP_ij) for the loss sum(O * dO)."""
@@ -220,3 +242,7 @@ def forward(Q, K, V, causal=False, scale=None):
 
 def backward(Q, K, V, dO, causal=False, scale=None):
     return default().backward(Q, K, V, dO, causal, scale)
+
+
+def probabilities(Q, K, causal=False, scale=None):
+    return default().probabilities(Q, K, causal, scale)

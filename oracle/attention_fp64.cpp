@@ -19,6 +19,9 @@
 //    flash_attention_backward docstring; the two matrix-calculus rules
 //    (O = PV and P = softmax(S)) in "Flash Attention" notes (page 3),
 //    section 1.5 "Matrix Calculus Cheatsheet".
+//  * the score and probability matrices themselves (S and P of standard
+//    attention, which the materialised baseline writes to memory) -- page 1,
+//    standard_attention.
 //  * the online (one-pass) max / rescaled-sum recurrence -- page 1,
 //    online_softmax_stats; page 3, section 1.1 "Online Softmax".
 //
@@ -139,6 +142,23 @@ int oracle_attention_forward_rows(const double* Q, const double* K, const double
         for (long c = 0; c < d; ++c) Oi[c] += p * V[j * d + c];
       }
     }
+  }
+  return 0;
+}
+
+// The intermediates of standard attention for one head ("05_flash_attention.py",
+// standard_attention): the score matrix S (n x m; -inf where the causal mask
+// hides a key) and P = softmax(S) row-wise (n x m; 0 where hidden), each row's
+// P_ij = exp(s_ij - L_i) with L_i the row's direct log-sum-exp.
+int oracle_attention_probabilities(const double* Q, const double* K, long n, long m, long d,
+                                   int causal, double scale, double* S, double* P) {
+  if (!Q || !K || !S || !P || n < 1 || m < 1 || d < 1) return -1;
+#pragma omp parallel for schedule(dynamic, 4)
+  for (long i = 0; i < n; ++i) {
+    double* si = S + i * m;
+    for (long j = 0; j < m; ++j) si[j] = score(Q, K, d, i, j, causal, scale);
+    const double Li = row_logsumexp(si, m);
+    for (long j = 0; j < m; ++j) P[i * m + j] = si[j] == kNegInf ? 0.0 : std::exp(si[j] - Li);
   }
   return 0;
 }

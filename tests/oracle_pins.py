@@ -387,6 +387,28 @@ def pin_sampled_rows(orc):
         _close(Ds, D, 1e-15, 1e-15, "sampled D")
 
 
+# --------------------------------------------------------------------------
+# S and P of standard attention: S against a library matrix product, P against
+# scipy's softmax with the causal entries removed; P V reproduces O.
+# --------------------------------------------------------------------------
+def pin_probabilities(orc):
+    rng = _rng(12)
+    for (n, m, d, causal, scale) in ((6, 9, 4, False, 0.4), (9, 9, 3, True, 0.7),
+                                     (8, 5, 5, True, 0.3)):
+        Q, K, V = rng.standard_normal((n, d)), rng.standard_normal((m, d)), rng.standard_normal((m, d))
+        S, P = orc.probabilities(Q, K, causal, scale)
+        ref = scale * (Q @ K.T)
+        hidden = np.arange(m)[None, :] > np.arange(n)[:, None] if causal else np.zeros((n, m), bool)
+        assert np.all(np.isneginf(S[hidden])), "masked scores must be -inf"
+        _close(S[~hidden], ref[~hidden], 1e-14, 1e-14, f"scores causal={causal}")
+        soft = scipy.special.softmax(np.where(hidden, -np.inf, ref), axis=1)
+        _close(P, soft, 1e-13, 1e-15, f"probabilities causal={causal}")
+        assert np.all(P[hidden] == 0.0)
+        O, _ = orc.forward(Q, K, V, causal, scale)
+        _close(P @ V, O, 1e-13, 1e-14, f"P V = O causal={causal}")
+
+
 ALL_PINS = [pin_golden, pin_online_stats, pin_softmax_identity_v, pin_causal_row0,
             pin_zero_query, pin_single_key, pin_finite_differences, pin_invariants,
-            pin_torch_autograd, pin_tiled_page1, pin_causal_nonsquare, pin_sampled_rows]
+            pin_torch_autograd, pin_tiled_page1, pin_causal_nonsquare, pin_sampled_rows,
+            pin_probabilities]

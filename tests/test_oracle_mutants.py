@@ -28,6 +28,7 @@ MUTANTS = {
     "dQ_wrong_operand": ("dQi[c] += scale * dS * K[j * d + c];",
                          "dQi[c] += scale * dS * Q[i * d + c];"),
     "O_wrong_weight": ("Oi[c] += p * V[j * d + c];", "Oi[c] += std::exp(s[j]) * V[j * d + c];"),
+    "P_unnormalised": ("std::exp(si[j] - Li);", "std::exp(si[j]);"),
 }
 
 

@@ -65,7 +65,8 @@ def test_cross_b8_h8_n1000_m3000_d64():
     Q, K, V, dO = wl.workload_inputs(w)
     got = parity.run_gpu(Q, K, V, dO, w.causal)
     heads = wl.sample_indices(w.heads, 8, 2000 + 5)
-    parity.check_heads(Q, K, V, dO, w.causal, got, heads=heads)
+    # Q, K ~ 3 N(0,1): a peaked softmax, O checked beyond its inherent bf16 rounding
+    parity.check_heads(Q, K, V, dO, w.causal, got, heads=heads, raw_o=False)
 
 
 # ------------------------------------------------------------------ edge shapes
@@ -157,7 +158,7 @@ def test_peaked_scores_and_custom_scale():
     Q, K, V, dO = wl.attention_inputs(1, 2, 300, 500, 128, seed=7100, qk_std=3.0)
     for causal in (False, True):
         got = parity.run_gpu(Q, K, V, dO, causal, scale=0.05)
-        parity.check_heads(Q, K, V, dO, causal, got, scale=0.05)
+        parity.check_heads(Q, K, V, dO, causal, got, scale=0.05, raw_o=False)
 
 
 def _growing_scores(B, H, n, m, d, growth, seed):
@@ -182,7 +183,8 @@ def test_growing_row_maximum(growth):
     Q, K, V, dO = _growing_scores(1, 2, 300, 700, 64, growth, seed=7950)
     for causal in (False, True):
         got = parity.run_gpu(Q, K, V, dO, causal)
-        parity.check_heads(Q, K, V, dO, causal, got)
+        # growth 40 concentrates each row's weight on its last keys (peaked)
+        parity.check_heads(Q, K, V, dO, causal, got, raw_o=growth < 10)
     Q, K, V, dO = _growing_scores(1, 1, 520, 520, 128, growth, seed=7960)
     for causal in (False, True):
         got = parity.run_gpu(Q, K, V, dO, causal)
