@@ -26,7 +26,7 @@ def _built():
 def test_single_head(w):
     Q, K, V, dO = wl.workload_inputs(w)
     got = parity.run_gpu(Q, K, V, dO, w.causal)
-    parity.check_heads(Q, K, V, dO, w.causal, got)
+    parity.check_heads(Q, K, V, dO, w.causal, got, raw_o=True)
 
 
 def test_b4_h16_n1024_d64_causal():
@@ -34,7 +34,7 @@ def test_b4_h16_n1024_d64_causal():
     Q, K, V, dO = wl.workload_inputs(w)
     got = parity.run_gpu(Q, K, V, dO, w.causal)
     heads = wl.sample_indices(w.heads, 8, 2000 + 2)
-    parity.check_heads(Q, K, V, dO, w.causal, got, heads=heads)
+    parity.check_heads(Q, K, V, dO, w.causal, got, heads=heads, raw_o=True)
 
 
 def test_llama_b2_h32_n4096_d128_causal():
@@ -42,7 +42,7 @@ def test_llama_b2_h32_n4096_d128_causal():
     Q, K, V, dO = wl.workload_inputs(w)
     got = parity.run_gpu(Q, K, V, dO, w.causal)
     heads = wl.sample_indices(w.heads, 2, 2000 + 3)
-    parity.check_heads(Q, K, V, dO, w.causal, got, heads=heads)
+    parity.check_heads(Q, K, V, dO, w.causal, got, heads=heads, raw_o=True)
     # every output finite everywhere
     for k, v in got.items():
         assert np.isfinite(v).all(), k
@@ -55,7 +55,7 @@ def test_long_b1_h16_n16384_d128_causal():
     heads = wl.sample_indices(w.heads, 2, 2000 + 4)
     q_rows = wl.sample_indices(w.n, 256, 3000 + 4)
     k_rows = wl.sample_indices(w.m, 256, 4000 + 4)
-    parity.check_sampled(Q, K, V, dO, w.causal, got, heads, q_rows, k_rows)
+    parity.check_sampled(Q, K, V, dO, w.causal, got, heads, q_rows, k_rows, raw_o=True)
     for k, v in got.items():
         assert np.isfinite(v).all(), k
 
@@ -65,8 +65,9 @@ def test_cross_b8_h8_n1000_m3000_d64():
     Q, K, V, dO = wl.workload_inputs(w)
     got = parity.run_gpu(Q, K, V, dO, w.causal)
     heads = wl.sample_indices(w.heads, 8, 2000 + 5)
-    # Q, K ~ 3 N(0,1): a peaked softmax, O checked beyond its inherent bf16 rounding
-    parity.check_heads(Q, K, V, dO, w.causal, got, heads=heads, raw_o=False)
+    # Q, K ~ 3 N(0,1): a peaked softmax, where no bf16 kernel meets the raw bound;
+    # O is checked beyond its inherent bf16 rounding (the raw figure is recorded)
+    parity.check_heads(Q, K, V, dO, w.causal, got, heads=heads)
 
 
 # ------------------------------------------------------------------ edge shapes
@@ -158,7 +159,7 @@ def test_peaked_scores_and_custom_scale():
     Q, K, V, dO = wl.attention_inputs(1, 2, 300, 500, 128, seed=7100, qk_std=3.0)
     for causal in (False, True):
         got = parity.run_gpu(Q, K, V, dO, causal, scale=0.05)
-        parity.check_heads(Q, K, V, dO, causal, got, scale=0.05, raw_o=False)
+        parity.check_heads(Q, K, V, dO, causal, got, scale=0.05)
 
 
 def _growing_scores(B, H, n, m, d, growth, seed):
@@ -183,8 +184,7 @@ def test_growing_row_maximum(growth):
     Q, K, V, dO = _growing_scores(1, 2, 300, 700, 64, growth, seed=7950)
     for causal in (False, True):
         got = parity.run_gpu(Q, K, V, dO, causal)
-        # growth 40 concentrates each row's weight on its last keys (peaked)
-        parity.check_heads(Q, K, V, dO, causal, got, raw_o=growth < 10)
+        parity.check_heads(Q, K, V, dO, causal, got)
     Q, K, V, dO = _growing_scores(1, 1, 520, 520, 128, growth, seed=7960)
     for causal in (False, True):
         got = parity.run_gpu(Q, K, V, dO, causal)
