@@ -239,3 +239,36 @@ def test_session_argument_errors(lib):
     lib.fa_session_destroy(None)  # a no-op
     assert lib.fa_session_step(None, FAKE, FAKE, FAKE, FAKE, 0, 0.125, FAKE, FAKE, FAKE, FAKE,
                                FAKE) == api.FA_ERR_INVALID_ARG
+
+
+def test_standard_forward_argument_errors(lib):
+    f = lib.fa_standard_forward
+    Q, K, V = FAKE, FAKE + (1 << 24), FAKE + (2 << 24)
+    S, P, O, L = FAKE + (3 << 24), FAKE + (4 << 24), FAKE + (5 << 24), FAKE + (6 << 24)
+
+    def call(**kw):
+        a = dict(Q=Q, K=K, V=V, B=1, H=1, n=8, m=8, d=64, causal=0, scale=0.125, S=S, P=P, O=O,
+                 L=L)
+        a.update(kw)
+        return f(a["Q"], a["K"], a["V"], a["B"], a["H"], a["n"], a["m"], a["d"], a["causal"],
+                 a["scale"], a["S"], a["P"], a["O"], a["L"], None)
+
+    assert call(Q=None) == api.FA_ERR_INVALID_ARG
+    assert call(S=None) == api.FA_ERR_INVALID_ARG
+    assert call(P=None) == api.FA_ERR_INVALID_ARG
+    assert call(n=0) == api.FA_ERR_INVALID_ARG
+    assert call(d=20) == api.FA_ERR_UNSUPPORTED_HEAD_DIM
+    assert call(scale=0.0) == api.FA_ERR_INVALID_ARG
+    assert call(S=S + 8) == api.FA_ERR_MISALIGNED
+    assert call(L=L + 2) == api.FA_ERR_MISALIGNED
+    assert call(P=S) == api.FA_ERR_INVALID_ARG          # S and P overlap
+    assert call(S=Q) == api.FA_ERR_INVALID_ARG          # an output over an input
+    assert call(n=65535 * 128 + 1) == api.FA_ERR_INVALID_ARG  # more query tiles than grid rows
+
+
+def test_standard_matrix_bytes(lib):
+    assert fa.fa_standard_matrix_bytes(1, 1, 8, 8) == 8 * 64 * 2      # m_pad = 64
+    assert fa.fa_standard_matrix_bytes(2, 3, 5, 64) == 2 * 3 * 5 * 64 * 2
+    assert fa.fa_standard_matrix_bytes(2, 3, 5, 65) == 2 * 3 * 5 * 128 * 2
+    assert fa.fa_standard_matrix_bytes(1, 1, 0, 8) == 0
+    assert fa.fa_standard_matrix_bytes(1, 1, 8, 0) == 0

@@ -55,3 +55,14 @@ def test_visible_pairs_counts_the_causal_triangle():
         for causal in (False, True):
             assert b.visible_pairs(n, m, causal) == brute(n, m, causal), (n, m, causal)
     assert b.visible_pairs(4096, 4096, True) * 64 == 537_001_984  # 5.37e8 at the benchmark shape
+
+
+def test_io_model_counts_the_score_matrices():
+    b = _bench()
+    m = b.io_model_bytes(1, 2, 1024, 1024, 128)
+    io = 2 * ((2 * 1024 + 2 * 1024) * 128 * 2 + 1024 * 4)      # Q, K, V, O bf16; L fp32
+    assert m["tiled"] == io
+    assert m["standard"] - m["tiled"] == 2 * 4 * 1024 * 1024 * 2  # write S, read S, write P, read P
+    rows = b.io_configs()
+    assert {r[3] for r in rows} == {1024, 4096, 16384}
+    assert all(r[1] * r[2] * r[3] in (r[3], b.IO_QUERY_ROWS) for r in rows)
