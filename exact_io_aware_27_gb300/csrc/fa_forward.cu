@@ -52,7 +52,11 @@ constexpr float kRescaleThreshold = 8.0f;  // base-2 units: P stays below 2^8
 template <int D>
 struct FwdCfg {
   static constexpr int BM = 128;                 // query rows per tile = TMEM lanes
-  static constexpr int TILES = 2;                // query tiles per CTA
+  // Query tiles per CTA. TMEM would hold a third at d = 64, but with the deal's
+  // wave quantization at the d = 64 workload sizes three tiles ran slower.
+  static constexpr int TILES = 2;
+  static constexpr int QUSES = (TILES + 1) / 2;  // ring uses holding an item's Q tiles
+  static constexpr int SOFT0 = (TILES == 3) ? 2 : 4;  // first softmax warp
   static constexpr int BN = 128;                 // keys per loaded block (two halves of 64)
   static constexpr int KCH = D / 64;             // 128-byte column chunks per row
   static constexpr int CHUNK = 128 * 128;        // bytes of one chunk of a 128-row tile
@@ -63,7 +67,7 @@ struct FwdCfg {
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = STAGES * TILE;
   static constexpr int OFF_EPI = 2 * STAGES * TILE;  // O staging, one area per softmax warp
-  static constexpr int OFF_BAR = OFF_EPI + 8 * kStoreStageBytes;
+  static constexpr int OFF_BAR = OFF_EPI + 4 * TILES * kStoreStageBytes;
   // barrier slots
   static constexpr int B_KVF = 0;                // + slot: the slot's copies landed
   static constexpr int B_KVE = STAGES;           // + slot: the slot may be refilled
@@ -79,11 +83,12 @@ struct FwdCfg {
   // TMEM columns: Q_t as bf16 pairs (the A operand of S_t = Q_t K^T), S_t of one
   // 64-key step (then P_t as bf16 pairs over its first 32 columns), O_t.
   static constexpr uint32_t COL_Q = 0;           // + (D / 2) * tile
-  static constexpr uint32_t COL_S = D;           // + 64 * tile
-  static constexpr uint32_t COL_O = D + 128;     // + D * tile
+  static constexpr uint32_t COL_S = 128;         // + 64 * tile
+  static constexpr uint32_t COL_O = 128 + 64 * TILES;  // + D * tile
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr int THREADS = 384;
+  static constexpr int THREADS = 32 * (SOFT0 + 4 * TILES);
   static_assert(COL_O + TILES * D <= TMEM_COLS, "TMEM budget");
+  static_assert((D / 2) * TILES <= COL_S, "TMEM budget");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
@@ -113,7 +118,7 @@ __device__ __forceinline__ int tile_steps(int q0, int n, int m, int causal) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                const FwdParams p) {
@@ -135,24 +140,31 @@ __global__ void __launch_bounds__(384, 1)
   const int n_items = p.num_pairs * p.BH;
   int n_mine = 0;
   while (snake_item(n_mine, cta, P) < n_items) ++n_mine;
-  // Item j: first query, head and 64-key steps of each tile (tile 0 always has some).
-  auto item = [&](int j, int& qs, int& bh, int& nh0, int& nh1) {
-    int pair;
-    grouped_tile(snake_item(j, cta, P), p.BH, p.num_pairs, p.group, pair, bh);
-    if (p.causal) pair = p.num_pairs - 1 - pair;
-    qs = pair * (C::TILES * C::BM);
-    nh0 = tile_steps(qs, p.n, p.m, p.causal);
-    nh1 = tile_steps(qs + C::BM, p.n, p.m, p.causal);
+  // Item j: first query, head and 64-key steps of each tile (tile 0 always has
+  // some); returns the steps of the longest tile.
+  auto item = [&](int j, int& qs, int& bh, int (&nht)[C::TILES]) {
+    int grp;
+    grouped_tile(snake_item(j, cta, P), p.BH, p.num_pairs, p.group, grp, bh);
+    if (p.causal) grp = p.num_pairs - 1 - grp;
+    qs = grp * (C::TILES * C::BM);
+    int nh = 0;
+#pragma unroll
+    for (int t = 0; t < C::TILES; ++t) {
+      nht[t] = tile_steps(qs + t * C::BM, p.n, p.m, p.causal);
+      nh = max(nh, nht[t]);
+    }
+    return nh;
   };
-  // Ring uses of item j: one for its two Q tiles, then one per 128-key block of K, V.
-  // Every role counts them (`ru`) and the steps of each tile identically.
+  // Ring uses of item j: QUSES for its Q tiles (tiles 2u and 2u + 1 in the K and V
+  // buffers of use u), then one per 128-key block of K, V. Every role counts them
+  // (`ru`) and the steps of each tile identically.
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&bar[C::B_KVF + s], 1);
       mbar_init(&bar[C::B_KVE + s], 1);
     }
-    mbar_init(&bar[C::B_IN], 256);
+    mbar_init(&bar[C::B_IN], 128 * C::TILES);
     for (int t = 0; t < C::TILES; ++t) {
       mbar_init(&bar[C::B_SF + t], 1);
       mbar_init(&bar[C::B_PF + t], 128);
@@ -183,10 +195,9 @@ __global__ void __launch_bounds__(384, 1)
       int ru = 0;
       bool ok = true;
       for (int j = 0; ok && j < n_mine; ++j) {
-        int qs, bh, nh0, nh1;
-        item(j, qs, bh, nh0, nh1);
-        const int nkb = (max(nh0, nh1) + 1) / 2;  // 128-key blocks
-        for (int u = 0; u <= nkb; ++u, ++ru) {
+        int qs, bh, nht[C::TILES];
+        const int nkb = (item(j, qs, bh, nht) + 1) / 2;  // 128-key blocks
+        for (int u = 0; u < C::QUSES + nkb; ++u, ++ru) {
           const int s = ru % C::STAGES;
           if (ru >= C::STAGES &&
               !mbar_wait(&bar[C::B_KVE + s], ((ru / C::STAGES) & 1) ^ 1, wc)) {
@@ -194,17 +205,20 @@ __global__ void __launch_bounds__(384, 1)
             break;
           }
           uint64_t* f = &bar[C::B_KVF + s];
-          mbar_arrive_expect_tx(f, 2 * C::TILE);
+          // Q tiles 2u, 2u + 1 (the second only if the CTA has it), or K and V
+          const bool q_use = u < C::QUSES;
+          const bool two = !q_use || 2 * u + 1 < C::TILES;
+          mbar_arrive_expect_tx(f, (two ? 2 : 1) * C::TILE);
 #pragma unroll
           for (int c = 0; c < C::KCH; ++c) {
             uint8_t* kdst = smem + C::OFF_K + s * C::TILE + c * C::CHUNK;
             uint8_t* vdst = smem + C::OFF_V + s * C::TILE + c * C::CHUNK;
-            if (u == 0) {
-              tma_load_3d(kdst, &tmQ, f, c * 64, qs, bh);
-              tma_load_3d(vdst, &tmQ, f, c * 64, qs + C::BM, bh);
+            if (q_use) {
+              tma_load_3d(kdst, &tmQ, f, c * 64, qs + 2 * u * C::BM, bh);
+              if (two) tma_load_3d(vdst, &tmQ, f, c * 64, qs + (2 * u + 1) * C::BM, bh);
             } else {
-              tma_load_3d(kdst, &tmK, f, c * 64, (u - 1) * C::BN, bh);
-              tma_load_3d(vdst, &tmV, f, c * 64, (u - 1) * C::BN, bh);
+              tma_load_3d(kdst, &tmK, f, c * 64, (u - C::QUSES) * C::BN, bh);
+              tma_load_3d(vdst, &tmV, f, c * 64, (u - C::QUSES) * C::BN, bh);
             }
           }
         }
@@ -222,15 +236,13 @@ __global__ void __launch_bounds__(384, 1)
     if (n_mine > 0) {
       constexpr uint32_t kIdescS = idesc_bf16_f32(128, 64, false, false);
       constexpr uint32_t kIdescO = idesc_bf16_f32(128, D, false, true);
-      int ru = 0, base0 = 0, base1 = 0;  // ring uses and steps of earlier items
+      int ru = 0;                 // ring uses of earlier items
+      int base[C::TILES] = {};    // each tile's steps in earlier items
       bool ok = true;
       for (int j = 0; ok && j < n_mine; ++j) {
-        int qs, bh, nh0, nh1;
-        item(j, qs, bh, nh0, nh1);
-        const int nh = max(nh0, nh1), nkb = (nh + 1) / 2;
-        const int nht[2] = {nh0, nh1};
-        const int base[2] = {base0, base1};
-        auto use_of = [&](int k) { return ru + 1 + (k >> 1); };  // ring use of step k's block
+        int qs, bh, nht[C::TILES];
+        const int nh = item(j, qs, bh, nht), nkb = (nh + 1) / 2;
+        auto use_of = [&](int k) { return ru + C::QUSES + (k >> 1); };  // ring use of step k's block
         auto scores = [&](int t, int k) {
           const uint64_t b_k = sdesc_sw128(
               smem_u32(smem + C::OFF_K + (use_of(k) % C::STAGES) * C::TILE + (k & 1) * C::HALF_ROWS),
@@ -256,12 +268,14 @@ __global__ void __launch_bounds__(384, 1)
         // the O_t += P_t V product that overwrites it waits for P_t, which its
         // softmax warps write only after that.)
         if (!warp_wait(&bar[C::B_IN], j & 1, wc)) { ok = false; break; }
-        if (lane == 0) mbar_arrive(&bar[C::B_KVE + ru % C::STAGES]);  // the Q slot is free
+        if (lane == 0)  // the Q slots are free
+          for (int u = 0; u < C::QUSES; ++u) mbar_arrive(&bar[C::B_KVE + (ru + u) % C::STAGES]);
         const int u1 = use_of(0);
         if (!warp_wait(&bar[C::B_KVF + u1 % C::STAGES], (u1 / C::STAGES) & 1, wc)) { ok = false; break; }
         tc_fence_after();
-        if (nh0 > 0) scores(0, 0);
-        if (nh1 > 0) scores(1, 0);
+#pragma unroll
+        for (int t = 0; t < C::TILES; ++t)
+          if (nht[t] > 0) scores(t, 0);
         for (int k = 0; ok && k < nh; ++k) {
           if (k + 1 < nh && ((k + 1) & 1) == 0) {  // step k+1 opens block (k+1)/2
             const int u = use_of(k + 1);
@@ -289,17 +303,17 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
         for (int t = 0; t < C::TILES; ++t)
           if (ok && nht[t] == 0) umma_commit_w(&bar[C::B_PVD + t]);
-        ru += 1 + nkb;
-        base0 += nh0;
-        base1 += nh1;
+        ru += C::QUSES + nkb;
+#pragma unroll
+        for (int t = 0; t < C::TILES; ++t) base[t] += nht[t];
       }
       umma_commit_w(&bar[C::B_DRAIN]);
       drain_wait(&bar[C::B_DRAIN], 0);
     }
-  } else if (warp >= 4) {
+  } else if (warp >= C::SOFT0) {
     // ------------------------------------------------------------ softmax
-    const int t = (warp - 4) >> 2;                 // query tile of this warpgroup
-    const int row = ((warp - 4) & 3) * 32 + lane;  // row in the tile = TMEM lane
+    const int t = (warp - C::SOFT0) >> 2;          // query tile of this warpgroup
+    const int row = (warp & 3) * 32 + lane;        // row in the tile = TMEM lane
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const uint32_t scol = lane_base + C::COL_S + 64 * t;
     const uint32_t ocol = lane_base + C::COL_O + D * t;
@@ -310,9 +324,10 @@ __global__ void __launch_bounds__(384, 1)
     // j ^ (row % 8)). The previous item's S_t products, the only readers of these
     // columns, are complete: this warp waited for each of them.
     auto move_q = [&](int rq) {
-      const int s = rq % C::STAGES;
-      if (!warp_wait(&bar[C::B_KVF + s], (rq / C::STAGES) & 1, wc)) return false;
-      const uint8_t* tile = smem + (t == 0 ? C::OFF_K : C::OFF_V) + s * C::TILE;
+      const int uq = rq + (t >> 1);  // the ring use holding Q_t
+      const int s = uq % C::STAGES;
+      if (!warp_wait(&bar[C::B_KVF + s], (uq / C::STAGES) & 1, wc)) return false;
+      const uint8_t* tile = smem + ((t & 1) == 0 ? C::OFF_K : C::OFF_V) + s * C::TILE;
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
         uint32_t v[32];
@@ -334,10 +349,9 @@ __global__ void __launch_bounds__(384, 1)
     };
     bool ok = n_mine == 0 || move_q(0);
     for (int j = 0; ok && j < n_mine; ++j) {
-      int qs, bh, nh0, nh1;
-      item(j, qs, bh, nh0, nh1);
-      const int nkb = (max(nh0, nh1) + 1) / 2;
-      const int nh_t = t == 0 ? nh0 : nh1;
+      int qs, bh, nht[C::TILES];
+      const int nkb = (item(j, qs, bh, nht) + 1) / 2;
+      const int nh_t = nht[t];
       const int qg = qs + t * C::BM + row;
       float m_ref = -INFINITY;  // reference maximum of S * scale * log2(e)
       float l_run = 0.f;        // sum of exp2(S * scale * log2(e) - m_ref)
@@ -431,20 +445,21 @@ __global__ void __launch_bounds__(384, 1)
       }
       // The next item's Q_t goes in before this item's O_t comes out, so that the
       // next item's first S products run while the O rows are written.
-      if (ok && j + 1 < n_mine && !move_q(ru + 1 + nkb)) ok = false;
+      if (ok && j + 1 < n_mine && !move_q(ru + C::QUSES + nkb)) ok = false;
       // ---------------------------------------------------------- epilogue
       if (ok && nh_t > 0) {
         if (!warp_wait(&bar[C::B_PVD + t], pvd_t & 1, wc)) { ok = false; break; }
         tc_fence_after();
         // O / l as bf16 through the warp's staging area and TMA (rows past n and
         // the zero columns past d are not written)
-        tmem_rows_store<D>(ocol, 1.f / l_run, smem + C::OFF_EPI + (warp - 4) * kStoreStageBytes,
-                           &tmO, 0, qs + t * C::BM + ((warp - 4) & 3) * 32, p.n, bh, p.d);
+        tmem_rows_store<D>(ocol, 1.f / l_run,
+                           smem + C::OFF_EPI + (warp - C::SOFT0) * kStoreStageBytes, &tmO, 0,
+                           qs + t * C::BM + (warp & 3) * 32, p.n, bh, p.d);
         if (qg < p.n) p.L[(size_t)bh * p.n + qg] = (m_ref + lg2(l_run)) * kLn2;
         tc_fence_before();  // O_t read out before the next item's products overwrite it
         ++pvd_t;
       }
-      ru += 1 + nkb;
+      ru += C::QUSES + nkb;
       base_t += nh_t;
     }
     if (lane == 0) bulk_wait_all();  // the stores have read the staging buffers
