@@ -7,8 +7,9 @@ hot path. The metric is fwd+bwd TFLOP/s counting 4*B*H*n*m*d per forward (halved
 under causal masking) and 2.5x that per backward. `value` times the steps with
 the inputs already on the device, replaying the step from a CUDA graph (--eager
 launches it from the host instead); `e2e` times the same step through the C-ABI
-host-buffer call fa_session_step (inputs copied in from pinned host memory and
-every output copied back, each step, inside the timed region).
+host-buffer calls fa_session_submit / fa_session_sync (inputs copied in from
+pinned host memory and every output copied back, each step, inside the timed
+region).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -424,29 +425,33 @@ def run_ours(args):
 
     e2e = None
     if not args.no_e2e:
-        # End to end through the C-ABI host-buffer call (fa_session_step): pinned
-        # host inputs in, forward + backward, every output back in host memory, each
-        # step; the session pipelines the copies and kernels over chunks of at most
-        # B*H/8 heads.
+        # End to end through the C-ABI host-buffer calls: pinned host inputs in,
+        # forward + backward, every output back in host memory, each step. Each step
+        # is submitted with fa_session_submit and the session pipelines the copies and
+        # kernels over chunks of at most B*H/4 heads, continuing across steps (the
+        # next step's copies in run while this step's copies out do);
+        # fa_session_sync after the last step waits for all outputs.
         hq, hk, hv, hdo = (t.pin_memory() for t in (Q, K, V, dO))
         ho, hl = torch.empty_like(hq).pin_memory(), torch.empty((B, H, n), dtype=torch.float32).pin_memory()
         hdq, hdk, hdv = (torch.empty_like(t).pin_memory() for t in (hq, hk, hv))
         h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
         d2h = sum(t.numel() * t.element_size() for t in (ho, hl, hdq, hdk, hdv))
-        chunk = max(1, -(-(B * H) // 8))
+        chunk = max(1, -(-(B * H) // 4))
         sess = fa.Session(B, H, n, m, d, chunk)
 
         def e2e_step():
-            sess.step(hq, hk, hv, hdo, w.causal, O=ho, L=hl, dQ=hdq, dK=hdk, dV=hdv)
+            sess.submit(hq, hk, hv, hdo, w.causal, O=ho, L=hl, dQ=hdq, dK=hdk, dV=hdv)
 
         e2e_steps = max(3, min(args.steps, 50))
         for _ in range(3):
             e2e_step()
+        sess.sync()
         torch.cuda.synchronize(dev)
         barrier()
-        t0 = time.perf_counter()  # the call returns once the outputs are in host memory
+        t0 = time.perf_counter()
         for _ in range(e2e_steps):
             e2e_step()
+        sess.sync()  # every step's outputs are in host memory
         e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
         sess.close()
         barrier()
@@ -454,7 +459,8 @@ def run_ours(args):
         e2e_value = weak_value(flops_step, world, e2e_ms)
         e2e = {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-               "api": f"fa_session_step, host buffers, chunks of at most {chunk} heads"}
+               "api": (f"fa_session_submit per step, fa_session_sync after the last; "
+                       f"host buffers, chunks of at most {chunk} heads")}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

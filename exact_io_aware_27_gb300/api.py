@@ -52,6 +52,8 @@ SIGNATURES = {
     "fa_session_create": (_I, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_P)]),
     "fa_session_destroy": (None, [_P]),
     "fa_session_step": (_I, [_P, _P, _P, _P, _P, _I, _F, _P, _P, _P, _P, _P]),
+    "fa_session_submit": (_I, [_P, _P, _P, _P, _P, _I, _F, _P, _P, _P, _P, _P]),
+    "fa_session_sync": (_I, [_P]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_get_device_status": (_I, [ctypes.POINTER(_I)]),
     "fa_version": (_I, []),
@@ -342,10 +344,11 @@ def fa_online_softmax_stats(x: torch.Tensor, m=None, l=None, stream=None):
 
 
 class Session:
-    """A host-buffer session (fa_session_create / fa_session_step / destroy): one
-    forward + backward step on CPU tensors, pipelined on the GPU over chunks of
-    `chunk_heads` heads. Inputs and outputs are CPU tensors (page-locked ones let
-    the copies run asynchronously); the device is the current CUDA device."""
+    """A host-buffer session (fa_session_create / fa_session_step, or
+    fa_session_submit and fa_session_sync / destroy): one forward + backward step
+    on CPU tensors, pipelined on the GPU over chunks of `chunk_heads` heads.
+    Inputs and outputs are CPU tensors (page-locked ones let the copies run
+    asynchronously); the device is the current CUDA device."""
 
     def __init__(self, B: int, H: int, n: int, m: int, d: int, chunk_heads: int):
         self.shape = (B, H, n, m, d)
@@ -356,7 +359,22 @@ class Session:
 
     def step(self, Q, K, V, dO, causal: bool = False, scale: float | None = None, O=None,
              L=None, dQ=None, dK=None, dV=None):
-        """O, L, dQ, dK, dV (CPU tensors, allocated here when not given)."""
+        """O, L, dQ, dK, dV (CPU tensors, allocated here when not given), in host
+        memory when the call returns."""
+        return self._run("fa_session_step", Q, K, V, dO, causal, scale, O, L, dQ, dK, dV)
+
+    def submit(self, Q, K, V, dO, causal: bool = False, scale: float | None = None, O=None,
+               L=None, dQ=None, dK=None, dV=None):
+        """Queues one step (fa_session_submit) and returns its O, L, dQ, dK, dV
+        tensors, which hold the results once sync() has returned. Until then the
+        inputs must stay unchanged and the outputs unread."""
+        return self._run("fa_session_submit", Q, K, V, dO, causal, scale, O, L, dQ, dK, dV)
+
+    def sync(self):
+        """Waits until every submitted step's outputs are in host memory."""
+        _check("fa_session_sync", lib().fa_session_sync(self._handle))
+
+    def _run(self, fn, Q, K, V, dO, causal, scale, O, L, dQ, dK, dV):
         B, H, n, m, d = self.shape
         for name, t, rows in (("Q", Q, n), ("K", K, m), ("V", V, m), ("dO", dO, n)):
             if (t.is_cuda or t.dtype != torch.bfloat16 or tuple(t.shape) != (B, H, rows, d)
@@ -372,11 +390,11 @@ class Session:
         dQ = new(Q) if dQ is None else _out("dQ", dQ, (B, H, n, d), bf, cpu)
         dK = new(K) if dK is None else _out("dK", dK, (B, H, m, d), bf, cpu)
         dV = new(V) if dV is None else _out("dV", dV, (B, H, m, d), bf, cpu)
-        rc = lib().fa_session_step(self._handle, Q.data_ptr(), K.data_ptr(), V.data_ptr(),
-                                   dO.data_ptr(), int(bool(causal)), _scale(scale, d),
-                                   O.data_ptr(), L.data_ptr(), dQ.data_ptr(), dK.data_ptr(),
-                                   dV.data_ptr())
-        _check("fa_session_step", rc)
+        rc = getattr(lib(), fn)(self._handle, Q.data_ptr(), K.data_ptr(), V.data_ptr(),
+                                dO.data_ptr(), int(bool(causal)), _scale(scale, d),
+                                O.data_ptr(), L.data_ptr(), dQ.data_ptr(), dK.data_ptr(),
+                                dV.data_ptr())
+        _check(fn, rc)
         return O, L, dQ, dK, dV
 
     def close(self):

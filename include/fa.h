@@ -212,7 +212,7 @@ FA_API int fa_online_softmax_stats(const float* x, long long rows, long long col
 /*
  * Host-buffer sessions: one forward + backward step whose inputs and outputs are
  * in host memory, for callers that keep their tensors on the host. A session owns
- * device buffers for `chunk_heads` heads at a time (three sets), a backward
+ * device buffers for `chunk_heads` heads at a time (four sets), a backward
  * workspace for one chunk and three CUDA streams (copies in, kernels, copies out)
  * on the device current when it is created.
  *
@@ -227,7 +227,7 @@ FA_API int fa_online_softmax_stats(const float* x, long long rows, long long col
  * to run asynchronously; pageable buffers work but serialise.
  *
  * fa_session_create: shapes and rules as fa_forward, 1 <= chunk_heads <= B*H.
- * It allocates device memory (the only entry point that does): three sets of
+ * It allocates device memory (the only entry point that does): four sets of
  * chunk_heads x (4 n d + 4 m d) bf16 values and chunk_heads x n fp32, plus one
  * workspace. Returns FA_OK and *out, or a negative fa_status (FA_ERR_CUDA if an
  * allocation fails; nothing is left allocated then).
@@ -241,6 +241,21 @@ FA_API int fa_online_softmax_stats(const float* x, long long rows, long long col
  * sees only their addresses. A session serves one thread at a time (its streams
  * and buffer sets are not shared safely by concurrent steps); separate sessions
  * may run concurrently.
+ * fa_session_submit: the same step, arguments and rules as fa_session_step, but
+ * it returns once the step's copies and kernels are queued. Steps submitted one
+ * after another continue one pipeline, so a step's copies in run while the
+ * previous step's copies out still do, and the link is busy in both directions
+ * across step boundaries. Until fa_session_sync returns, the caller must leave
+ * the step's input buffers unchanged and must not read or reuse its output
+ * buffers for anything else (two submitted steps may share input buffers, and
+ * may share output buffers when the caller reads only the last step's results:
+ * the copies out run in submission order). Host buffers must be page-locked for
+ * the call to return before the copies finish. Returns FA_OK or the first error
+ * while queuing; kernel timeouts are reported by fa_get_device_status().
+ * fa_session_sync: waits until every step submitted on the session has its
+ * outputs in host memory. Returns FA_OK, FA_ERR_INVALID_ARG for a NULL session,
+ * or FA_ERR_CUDA. fa_session_step is fa_session_submit followed by
+ * fa_session_sync.
  */
 typedef struct fa_session fa_session;
 FA_API int fa_session_create(int B, int H, int n, int m, int d, int chunk_heads,
@@ -249,6 +264,10 @@ FA_API void fa_session_destroy(fa_session* s);
 FA_API int fa_session_step(fa_session* s, const void* Q, const void* K, const void* V,
                            const void* dO, int causal, float scale, void* O, float* L,
                            void* dQ, void* dK, void* dV);
+FA_API int fa_session_submit(fa_session* s, const void* Q, const void* K, const void* V,
+                             const void* dO, int causal, float scale, void* O, float* L,
+                             void* dQ, void* dK, void* dV);
+FA_API int fa_session_sync(fa_session* s);
 
 /* A static, human-readable name for a status code. Never NULL. */
 FA_API const char* fa_status_string(int status);

@@ -239,6 +239,9 @@ def test_session_argument_errors(lib):
     lib.fa_session_destroy(None)  # a no-op
     assert lib.fa_session_step(None, FAKE, FAKE, FAKE, FAKE, 0, 0.125, FAKE, FAKE, FAKE, FAKE,
                                FAKE) == api.FA_ERR_INVALID_ARG
+    assert lib.fa_session_submit(None, FAKE, FAKE, FAKE, FAKE, 0, 0.125, FAKE, FAKE, FAKE, FAKE,
+                                 FAKE) == api.FA_ERR_INVALID_ARG
+    assert lib.fa_session_sync(None) == api.FA_ERR_INVALID_ARG
 
 
 def test_standard_forward_argument_errors(lib):

@@ -59,3 +59,34 @@ def test_session_rejects_device_or_misshaped_inputs():
             sess.step(Q[:, :1].contiguous(), K, V, dO)
     finally:
         sess.close()
+
+
+@pytest.mark.parametrize("B,H,n,m,d,causal,chunk", [
+    (2, 3, 300, 257, 64, True, 4),     # 2 chunks a step: buffer sets reused across steps
+    (1, 8, 513, 513, 128, True, 3),    # 4 chunks a step
+    (1, 1, 200, 77, 64, False, 1),     # 1 chunk a step
+])
+def test_submitted_steps_overlap_and_match(B, H, n, m, d, causal, chunk):
+    """Three steps submitted back to back, each on its own inputs and into its own
+    output buffers, then one sync: each step's outputs equal the device path's for
+    its inputs, so the pipeline that continues across steps keeps every chunk's
+    buffer set apart from its neighbours' and from the previous step's."""
+    batches = [wl.attention_inputs(B, H, n, m, d, seed=8500 + 10 * i + n) for i in range(3)]
+    refs = [_device_reference(*b, causal, None) for b in batches]
+    sess = fa.Session(B, H, n, m, d, chunk)
+    try:
+        outs = []
+        for b in batches:
+            pinned = [t.pin_memory() for t in b]
+            outs.append((pinned, sess.submit(*pinned, causal=causal)))
+        sess.sync()
+        for i, ((_, got), ref) in enumerate(zip(outs, refs)):
+            for name, a, r in zip(("O", "L", "dQ", "dK", "dV"), got, ref):
+                assert torch.equal(a, r), f"step {i} {name}"
+        # a blocking step after submitted ones continues the same pipeline
+        got = sess.step(*[t.pin_memory() for t in batches[0]], causal=causal)
+        for name, a, r in zip(("O", "L", "dQ", "dK", "dV"), got, refs[0]):
+            assert torch.equal(a, r), name
+    finally:
+        sess.close()
+    assert fa.fa_get_device_status() == 0
