@@ -154,6 +154,27 @@ def test_other_head_dims(B, H, n, m, d, causal):
     parity.check_heads(Q, K, V, dO, causal, got)
 
 
+# A seeded sweep of random shapes: batch and head counts, ragged query and key lengths
+# (one row up to several tiles, either longer), every supported head-dimension class
+# and both masks, so that tile and step boundaries fall at arbitrary offsets.
+def _random_shapes(count, seed):
+    rng = np.random.RandomState(seed)
+    out = []
+    for _ in range(count):
+        B, H = int(rng.randint(1, 4)), int(rng.randint(1, 5))
+        n, m = int(rng.randint(1, 701)), int(rng.randint(1, 701))
+        d = int(8 * rng.randint(1, 17))
+        out.append((B, H, n, m, d, bool(rng.randint(0, 2))))
+    return out
+
+
+@pytest.mark.parametrize("B,H,n,m,d,causal", _random_shapes(40, 7900))
+def test_random_shapes(B, H, n, m, d, causal):
+    Q, K, V, dO = wl.attention_inputs(B, H, n, m, d, seed=7900 + n + 7 * m + d, qk_std=1.0)
+    got = parity.run_gpu(Q, K, V, dO, causal)
+    parity.check_heads(Q, K, V, dO, causal, got)
+
+
 def test_peaked_scores_and_custom_scale():
     # Q, K ~ 3 N(0,1): peaked softmax, large row maxima; non-default scale
     Q, K, V, dO = wl.attention_inputs(1, 2, 300, 500, 128, seed=7100, qk_std=3.0)
